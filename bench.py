@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the batched tree speculative-sampling verify step on GB300.
+
+One step = one spec_verify_tree call (tree preparation, dense row pass, accept
+walk) over one batch of synthetic, seeded trees whose logits are already resident
+in HBM.  The headline workload is B=64 trees of 60 nodes over V=128256 bf16 logits
+(T=0.7, top-p 0.9); its target and draft logits (1.97 GB) are larger than the L2,
+so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead
+(rank 0 only; other ranks exit 0).  Under torchrun each rank verifies its own
+batch of trees (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_spec_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verified draft-node logit rows/sec and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "rows/s"
+DEFAULT_WORKLOAD = "tree60_b64_v128256"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ROW_PASS_SOURCES = ["speculative_decoding_tree_spec_gb300/csrc/rows.cu",
+                    "speculative_decoding_tree_spec_gb300/csrc/common.cuh",
+                    "speculative_decoding_tree_spec_gb300/csrc/internal.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=20261202)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (small cases for profiling)")
+    ap.add_argument("--e2e-steps", type=int, default=12)
+    ap.add_argument("--cpu-trees", type=int, default=48,
+                    help="tree-steps in the oracle sample of the cpu_baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own independent batch of trees."""
+    return seed + 1000003 * rank
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, profiles
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons in a background thread."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid]
+        except Exception:
+            sel = []
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+               f"-lms={period_ms}"] + sel
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        rows = [s for t, s in self.samples if t0 <= t <= t1 and len(s) == len(self.FIELDS)]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"], r[3:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        power = [num(r[2]) for r in rows if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def sources_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM traffic of the row pass from the committed ncu summary, if it was
+    captured on the current row-pass sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"row_pass_{workload}.md")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"row_pass_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not d:
+        return None, None
+    if d.group(1) != sources_digest(ROW_PASS_SOURCES):
+        return None, "stale"
+    return float(m.group(1)), "current"
+
+
+# ---------------------------------------------------------------------------
+# the oracle leg (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_pool(w, seed, n_trees, device):
+    """Host copies of n_trees trees of workload w (the oracle's input format)."""
+    small = w.with_(B=n_trees)
+    inp = wl.build_inputs(small, seed=seed, device=device)
+    return {"p": wl.host_logits(inp["p"]), "q": wl.host_logits(inp["q"]),
+            "tokens": inp["tokens"], "parents": inp["parents"], "max_depth": inp["max_depth"]}
+
+
+def time_oracle(w, pool, n_steps, threads, seed):
+    """n_steps tree-steps (step k verifies pool tree k mod P, drawing as batch index k)
+    on `threads` host threads.  Returns (wall seconds, rows verified)."""
+    import oracle
+
+    P = pool["p"].shape[0]
+
+    def step(k):
+        j = k % P
+        oracle.verify_tree(pool["p"][j:j + 1], pool["q"][j:j + 1], pool["tokens"][j:j + 1],
+                           pool["parents"][j:j + 1], pool["max_depth"], w.temperature, w.top_k,
+                           w.top_p, seed=seed, offset=0, batch_index=k)
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(step, range(n_steps)))
+    return time.perf_counter() - t0, n_steps * w.N
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    threads = os.cpu_count() or 1
+    pool = oracle_pool(w, args.seed, min(16, w.B), "cpu")
+    time_oracle(w, pool, args.warmup, threads, args.seed)
+    wall, rows = time_oracle(w, pool, args.steps, threads, args.seed)
+    value = rows / wall
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "V": w.V, "logits": w.dtype,
+                   "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
+                   "step": "one tree verified by the CPU oracle (steps run on a host thread pool)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} tree-steps cycling over {pool['p'].shape[0]} "
+                                   f"seeded trees of {w.name}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    if w.logits == "lmhead":
+        raise SystemExit("the fused LM-head workload is not wired into bench.py yet")
+    seed = shard_seed(args.seed, rank)
+    inp = wl.build_inputs(w, seed=seed, device=dev)
+    tok = torch.as_tensor(inp["tokens"], device=dev)
+    par = torch.as_tensor(inp["parents"], device=dev)
+    call = binding.PreparedVerify(inp["p"], inp["q"], tok, par, inp["max_depth"], w.temperature,
+                                  w.top_k, w.top_p, seed=seed, offset=0)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call()
+    counters = call.read_counters()
+    acc = call.out["accept_len"].cpu().numpy()
+    tokens_per_step = int((acc + 1).sum())
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.wait_first()
+    K = args.steps
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    row_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    row_end = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(K):
+        call(binding.SPEC_PHASE_PREPARE)
+        row_start[k].record(stream)
+        call(binding.SPEC_PHASE_ROWS)
+        row_end[k].record(stream)
+        call(binding.SPEC_PHASE_WALK)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    row_ms = [row_start[k].elapsed_time(row_end[k]) for k in range(K)]
+    row_avg_ms = sum(row_ms) / K
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    rows_per_step = w.B * w.N
+    value = world * rows_per_step * K / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / K
+
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = counters["dense_bytes"] / (row_avg_ms / 1e3) / 1e9
+    traffic, traffic_state = profiled_traffic(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic,
+                "kernel": "row_pass_kernel (dense row pass)",
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": counters["dense_bytes"],
+                "avg_launch_ms": row_avg_ms}
+    if traffic_state == "stale":
+        roofline["traffic_note"] = "ncu capture predates the current row-pass sources"
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "V": w.V, "logits": w.dtype,
+                   "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
+                   "tree": f"{w.tree}, depth {inp['max_depth']}, branching <= {w.max_branch}",
+                   "rng_offset": "fixed per step",
+                   "l2": f"inputs {2 * w.B * w.N * w.V * (2 if w.dtype == 'bf16' else 4) / 1e9:.2f}"
+                         " GB per step, larger than L2; no flush",
+                   "parallelism": f"weak: {world} rank(s) x {w.B} trees"},
+        "tokens_per_s": world * tokens_per_step * K / (elapsed_ms / 1e3),
+        "step_hbm_gbs": (counters["dense_bytes"] + counters["walk_bytes"]) / (ms_per_step / 1e3) / 1e9,
+        "work_per_step": counters,
+        "roofline": roofline,
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, w, inp, dev, stream)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = run_cpu_baseline(args, w, inp)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, w, inp, dev, stream):
+    """The same metric through the public C-ABI call with host buffers: every step
+    copies the inputs host->device from pinned memory, verifies, and copies the
+    accepted lengths, tokens and paths back."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    host = {k: inp[k].cpu().pin_memory() for k in ("p", "q")}
+    host["tokens"] = torch.as_tensor(inp["tokens"]).pin_memory()
+    host["parents"] = torch.as_tensor(inp["parents"]).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    call = binding.PreparedVerify(dbuf["p"], dbuf["q"], dbuf["tokens"], dbuf["parents"],
+                                  inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=1, offset=0)
+    outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+            for k, v in call.out.items() if k in ("accept_len", "tokens", "path")}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        call()
+        for k, v in outs.items():
+            v.copy_(call.out[k], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.e2e_steps
+    world = dist_env()[0]
+    ms = max_over_ranks(ms, world, dev)
+    return {"value": world * w.B * w.N / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": args.e2e_steps}
+
+
+def run_cpu_baseline(args, w, inp):
+    import oracle
+
+    oracle.build()
+    n_pool = min(16, w.B)
+    idx = torch.arange(n_pool, device=inp["p"].device)
+    pool = {"p": wl.host_logits(inp["p"].index_select(0, idx)),
+            "q": wl.host_logits(inp["q"].index_select(0, idx)),
+            "tokens": inp["tokens"][:n_pool], "parents": inp["parents"][:n_pool],
+            "max_depth": inp["max_depth"]}
+    threads = os.cpu_count() or 1
+    wall, rows = time_oracle(w, pool, args.cpu_trees, threads, args.seed)
+    return {"value": rows / wall, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{args.cpu_trees} tree-steps cycling over the first {n_pool} trees of "
+                      f"the timed batch ({w.name}), one tree per host thread task"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

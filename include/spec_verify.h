@@ -1,0 +1,209 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched tree speculative-sampling
+ * verify library (EAGLE / SpecInfer style).
+ *
+ * What the operation is (sources cited by page and section):
+ *   - p and q are compared after temperature / top-k / top-p / argmax processing
+ *     ("LLM speculative decoding: EAGLE", jingming.pro, section 1 note);
+ *   - a drafted token x is accepted with probability min(1, p(x)/q(x)); after a
+ *     rejection p becomes norm(max(0, p - q)); if every candidate is rejected the
+ *     token is resampled from that adjusted distribution, and if every drafted
+ *     token along the path is accepted one bonus token is sampled from the next
+ *     p (same page, section 2.3 steps 3-5);
+ *   - on a draft tree the sampler is applied recursively at every node, trying
+ *     the next sibling after a rejection (EAGLE / EAGLE-2 translation,
+ *     modelers.csdn.net, sections 1.3.2 and 1.7);
+ *   - at temperature 0 the drafted tokens are compared with the target argmax
+ *     ("EAGLE close reading", edgeai1.github.io, sections 3 and 5).
+ *
+ * Conventions shared by every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller, unless stated.
+ *     The library allocates nothing and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
+ *     and returns before the GPU work finishes; it never synchronises the device.
+ *   - The return value is SPEC_OK (0) or a negative SPEC_ERR_* code.  Argument
+ *     errors are detected on the host before anything is launched.  Conditions
+ *     that depend on device-resident data (a malformed tree, a NaN logit) are
+ *     reported per tree in out_status instead.
+ *   - Logits are row-major; element (b, n, v) lives at
+ *     base + b * batch_stride + n * row_pitch + v (strides in elements).  The base
+ *     pointer must be 16-byte aligned and row_pitch * sizeof(elem) and
+ *     batch_stride * sizeof(elem) multiples of 16 bytes (batch_stride may be 0:
+ *     every tree then reads the same rows).
+ *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
+ *     {seed_lo, seed_hi} and counter {node, b, offset_lo, offset_hi}; word 0 is
+ *     the accept test of a child node, word 1 the final draw at a node; the
+ *     uniform is ((x >> 8) + 1) * 2^-24 in (0, 1].  The same arguments therefore
+ *     reproduce the same result bit for bit; callers advance rng_offset per round.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Sampling transforms applied identically to the target row p and the draft row q,
+ * in the order temperature -> top-k -> top-p.  Ranking is by raw logit with ties
+ * to the lower vocabulary index; top-p keeps the shortest rank-order prefix of the
+ * top-k set whose renormalised mass is >= top_p. */
+typedef struct {
+  float temperature; /* 0: greedy (argmax); > 0: sampling at this temperature */
+  int32_t top_k;     /* <= 0 or >= V: off */
+  float top_p;       /* >= 1: off; must be > 0 */
+  uint32_t flags;    /* SPEC_FLAG_* bits */
+} spec_sampling_params;
+
+/* Select the top-k / top-p cut with the full-row radix selection even where the
+ * single-pass candidate window would do (both give identical results). */
+#define SPEC_FLAG_EXACT_SELECT 1u
+
+/* Return codes. */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)
+#define SPEC_ERR_UNSUPPORTED_DTYPE (-2)
+#define SPEC_ERR_MISALIGNED (-3)
+#define SPEC_ERR_WORKSPACE (-4)
+#define SPEC_ERR_CUDA (-5)
+#define SPEC_ERR_TOO_LARGE (-6)
+
+/* Per-tree status written to out_status. */
+#define SPEC_TREE_OK 0
+#define SPEC_ROW_NONFINITE 1 /* a row the walk needed holds NaN or +inf, or is all -inf */
+#define SPEC_TREE_INVALID 2  /* parent_idx / draft_tokens malformed, or depth > max_depth */
+
+/* Size limits checked on the host. */
+#define SPEC_MAX_NODES 4096
+#define SPEC_MAX_VOCAB (1 << 21)
+
+/* Statistics of one filtered row (32 bytes).  For a kept token x,
+ *   P(x) = exp((z_x - m) / T) / s_f;
+ * token x is kept iff key(z_x) > cut_key, or key(z_x) == cut_key and x <= cut_idx,
+ * where key() is the order-preserving unsigned image of the fp32 logit
+ * (sign bit set -> all bits flipped, else sign bit set; -0 counts as +0).
+ * When nothing is truncated (T > 0, top-k and top-p off) every token is kept and
+ * the row reports cut_key = 0, cut_idx = V - 1, kept = V. */
+typedef struct {
+  float m;          /* maximum logit of the row */
+  int32_t status;   /* SPEC_TREE_OK or SPEC_ROW_NONFINITE */
+  double s_f;       /* sum over kept tokens of exp((z - m) / T); 1 at T == 0 */
+  uint32_t cut_key; /* key of the last kept token in rank order */
+  int32_t cut_idx;  /* vocabulary index of that token */
+  int32_t argmax;   /* lowest index of the maximum logit */
+  int32_t kept;     /* number of kept tokens */
+} spec_row_stats;
+
+/* Work counters of one spec_verify_tree call (algorithmic, not measured bytes). */
+typedef struct {
+  uint64_t dense_rows;      /* logit rows read by the dense row pass */
+  uint64_t dense_bytes;     /* bytes of those rows */
+  uint64_t walk_bytes;      /* row bytes read by residual and final-draw passes */
+  uint64_t residual_passes; /* rejections that renormalised max(0, p - q) */
+  uint64_t final_draws;     /* inverse-CDF draws (corrections and bonus tokens) */
+  uint64_t fallback_rows;   /* rows whose cut needed the full-row radix selection */
+  uint64_t reserved[2];
+} spec_verify_counters;
+
+/* Bytes of device workspace spec_verify_tree needs for B trees of N nodes over a
+ * vocabulary of V (the dtype does not change it).  Returns 0 for invalid sizes. */
+size_t spec_verify_workspace_size(int32_t B, int32_t N, int32_t V, spec_dtype dtype);
+
+/*
+ * Verify B draft trees of N nodes each (node 0 = root, the last accepted prefix
+ * token's position; nodes 1..N-1 are drafts).
+ *
+ * logits_p [B, N, V]: target logits; row n is the target's next-token distribution
+ *   after the path root..n.  logits_q [B, N, V]: draft logits; row n is the draft
+ *   distribution the children of n were drawn from (siblings share it).  logits_q
+ *   may be NULL when temperature == 0 (greedy never reads it).
+ * draft_tokens [B, N] int32: token of node n (entry 0 is ignored).
+ * parent_idx [B, N] int32: parent of node n; parent_idx[b][0] == -1 and
+ *   0 <= parent_idx[b][n] < n for n >= 1.  Trees may differ across b.
+ * max_depth: the deepest node of any tree is at most this deep; it sets the
+ *   output width W = max_depth + 1.
+ * Outputs (device, caller-owned):
+ *   out_accept_len [B]: accepted draft tokens (0..depth), -1 for a failed tree;
+ *   out_tokens [B, W]: the accepted tokens, then the correction / bonus token,
+ *     then -1 padding;
+ *   out_accepted_path [B, W]: node 0, then the accepted nodes, then -1 padding;
+ *   out_alpha [B, N] (optional, may be NULL): the acceptance probability used for
+ *     every tested node, NaN for untested nodes (greedy: 1 accept, 0 reject);
+ *   out_status [B] (optional): SPEC_TREE_OK / SPEC_ROW_NONFINITE / SPEC_TREE_INVALID;
+ *   out_counters (optional): work counters of this call.
+ * workspace: device scratch of at least spec_verify_workspace_size() bytes,
+ *   256-byte aligned; its contents are not preserved between calls.
+ * Errors: SPEC_ERR_INVALID_ARG (null required pointer, negative or inconsistent
+ *   sizes, non-finite or negative temperature, top_p <= 0, unknown flags),
+ *   SPEC_ERR_UNSUPPORTED_DTYPE, SPEC_ERR_MISALIGNED, SPEC_ERR_WORKSPACE (too small
+ *   or misaligned), SPEC_ERR_TOO_LARGE (N > SPEC_MAX_NODES, V > SPEC_MAX_VOCAB),
+ *   SPEC_ERR_CUDA (a launch failed).  B == 0 launches nothing and returns SPEC_OK.
+ */
+int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtype, int32_t B,
+                     int32_t N, int32_t V, int64_t row_pitch, int64_t batch_stride,
+                     const int32_t* draft_tokens, const int32_t* parent_idx, int32_t max_depth,
+                     spec_sampling_params params, uint64_t rng_seed, uint64_t rng_offset,
+                     int32_t* out_accept_len, int32_t* out_tokens, int32_t* out_accepted_path,
+                     float* out_alpha, int32_t* out_status, spec_verify_counters* out_counters,
+                     void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Phases of one verify call, for spec_verify_tree_phases. */
+#define SPEC_PHASE_PREPARE 1u /* validate the trees, build child lists, mark needed q rows */
+#define SPEC_PHASE_ROWS 2u    /* dense row pass: row statistics of every p and needed q row */
+#define SPEC_PHASE_WALK 4u    /* the accept walk, residual renormalisation and final draw */
+#define SPEC_PHASE_ALL 7u
+
+/*
+ * spec_verify_tree split into its phases: the phases whose bits are set in
+ * `phases` are launched, in the order prepare -> rows -> walk.  Calling it with
+ * SPEC_PHASE_PREPARE, then SPEC_PHASE_ROWS, then SPEC_PHASE_WALK on one stream with
+ * identical arguments and the same workspace is equivalent to one spec_verify_tree
+ * call (which is spec_verify_tree_phases with SPEC_PHASE_ALL); a caller can record
+ * events or enqueue other work between the phases.  The workspace carries the state
+ * between phases.  Errors as spec_verify_tree; an unknown phase bit or phases == 0
+ * is SPEC_ERR_INVALID_ARG.
+ */
+int spec_verify_tree_phases(uint32_t phases, const void* logits_p, const void* logits_q,
+                            spec_dtype dtype, int32_t B, int32_t N, int32_t V, int64_t row_pitch,
+                            int64_t batch_stride, const int32_t* draft_tokens,
+                            const int32_t* parent_idx, int32_t max_depth,
+                            spec_sampling_params params, uint64_t rng_seed, uint64_t rng_offset,
+                            int32_t* out_accept_len, int32_t* out_tokens,
+                            int32_t* out_accepted_path, float* out_alpha, int32_t* out_status,
+                            spec_verify_counters* out_counters, void* workspace,
+                            size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * The dense row pass alone: filter R rows (row r at logits + r * row_pitch
+ * elements) with `params` and write one spec_row_stats per row to out_stats
+ * (device, [R]).  Same transforms as spec_verify_tree ("LLM speculative decoding:
+ * EAGLE", section 1 note).  Needs no workspace.  Errors as spec_verify_tree.
+ */
+int spec_filter_rows(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
+                     int64_t row_pitch, spec_sampling_params params, spec_row_stats* out_stats,
+                     spec_stream_t stream);
+
+/*
+ * The Philox4x32-10 words the verify step draws: for i < n, the four 32-bit words
+ * of Philox(key = seed, counter = {node_idx[i], b_idx[i], offset_lo, offset_hi})
+ * go to out_words[4 i .. 4 i + 3].  b_idx, node_idx, out_words are device arrays.
+ */
+int spec_philox_words(uint64_t seed, uint64_t offset, const int32_t* b_idx,
+                      const int32_t* node_idx, int32_t n, uint32_t* out_words,
+                      spec_stream_t stream);
+
+/* Static description of a return code (never NULL). */
+const char* spec_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

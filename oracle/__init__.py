@@ -82,7 +82,8 @@ def _load():
             lib.oracle_verify_tree.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int64, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_double,
-                ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64, P, P,
+                ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32,
+                P, P,
                 P, P, P, P, P, P, P, ctypes.c_int]
             lib.oracle_verify_tree.restype = ctypes.c_int
             _lib = lib
@@ -145,11 +146,12 @@ def filter_rows(rows, temperature: float, top_k: int, top_p: float, want_probs: 
 def verify_tree(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
                 temperature: float, top_k: int, top_p: float, seed: int, offset: int = 0,
                 u_accept=None, u_final=None, want_final_dist: bool = False,
-                batch_broadcast: bool = False, nthreads: int = 1):
+                batch_broadcast: bool = False, nthreads: int = 1, batch_index: int = 0):
     """Run the oracle walk on B trees.
 
     logits_p / logits_q: [B, N, V] (or [N, V] with batch_broadcast=True, shared by
     every tree) float32 or raw-bf16 uint16.  draft_tokens / parent_idx: [B, N] int32.
+    Tree b draws its uniforms as batch index batch_index + b.
     Returns a dict of numpy arrays: accept_len [B], tokens [B, D+1], path [B, D+1],
     alpha [B, N], status [B], near [B] and optionally final_dist [B, V].
     """
@@ -189,7 +191,7 @@ def verify_tree(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
     _load().oracle_verify_tree(
         _ptr(p), _ptr(q), dt, B, N, V, V, batch_stride, _ptr(tokens), _ptr(parent),
         int(max_depth), float(temperature), int(top_k), float(top_p), int(seed) & (2**64 - 1),
-        int(offset) & (2**64 - 1), _ptr(ua), _ptr(uf), _ptr(out["accept_len"]),
+        int(offset) & (2**64 - 1), int(batch_index), _ptr(ua), _ptr(uf), _ptr(out["accept_len"]),
         _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["alpha"]), _ptr(out["status"]),
         _ptr(out["near"]), _ptr(out.get("final_dist")), int(nthreads))
     return out

@@ -257,6 +257,7 @@ typedef struct {
   double T, top_p;
   int top_k;
   uint64_t seed, offset;
+  int32_t rng_b0;
   const double* u_accept;
   const double* u_final;
   int32_t* out_accept_len;
@@ -402,7 +403,7 @@ static void walk_one_tree(const walk_args* a, int b) {
       else
         alpha = (P[x] > 0.0) ? 1.0 : 0.0;
       double r = a->u_accept ? a->u_accept[(int64_t)b * N + c]
-                             : oracle_uniform(a->seed, a->offset, b, c, 0);
+                             : oracle_uniform(a->seed, a->offset, a->rng_b0 + b, c, 0);
       if (a->out_alpha) a->out_alpha[(int64_t)b * N + c] = alpha;
       if (fabs(r - alpha) < ORACLE_NEAR) near = 1;
       if (r <= alpha) {
@@ -425,7 +426,8 @@ static void walk_one_tree(const walk_args* a, int b) {
     }
     /* No child accepted (or u is a leaf): draw the correction / bonus token from
        the current p ([tutorial] section 2.3 step 4, both cases). */
-    double r = a->u_final ? a->u_final[(int64_t)b * N + u] : oracle_uniform(a->seed, a->offset, b, u, 1);
+    double r = a->u_final ? a->u_final[(int64_t)b * N + u]
+                          : oracle_uniform(a->seed, a->offset, a->rng_b0 + b, u, 1);
     final_tok = inverse_cdf(P, V, r, &near);
     if (a->out_final_dist) {
       double* fd = a->out_final_dist + (int64_t)b * V;
@@ -462,7 +464,9 @@ static void* walk_slice_main(void* arg) {
 
 /*
  * Verify B draft trees.  Logit element (b, n, v) sits at
- * b * batch_stride + n * row_pitch + v.  u_accept / u_final, when non-NULL,
+ * b * batch_stride + n * row_pitch + v.  Tree b draws its uniforms as batch
+ * index rng_b0 + b (so a slice of a larger batch reproduces the same draws).
+ * u_accept / u_final, when non-NULL,
  * replace the Philox uniforms ([B, N] each, indexed by the tested child /
  * the node of the final draw).  out_alpha [B, N] (NaN where untested),
  * out_near [B], out_final_dist [B, V] are optional.  Returns 0.
@@ -470,12 +474,13 @@ static void* walk_slice_main(void* arg) {
 int oracle_verify_tree(const void* logits_p, const void* logits_q, int dtype, int B, int N, int V,
                        int64_t row_pitch, int64_t batch_stride, const int32_t* draft_tokens,
                        const int32_t* parent_idx, int max_depth, double temperature, int top_k,
-                       double top_p, uint64_t seed, uint64_t offset, const double* u_accept,
+                       double top_p, uint64_t seed, uint64_t offset, int32_t rng_b0,
+                       const double* u_accept,
                        const double* u_final, int32_t* out_accept_len, int32_t* out_tokens,
                        int32_t* out_path, double* out_alpha, int32_t* out_status, int32_t* out_near,
                        double* out_final_dist, int nthreads) {
   walk_args a = {logits_p, logits_q, dtype, B, N, V, row_pitch, batch_stride, draft_tokens,
-                 parent_idx, max_depth, temperature, top_p, top_k, seed, offset, u_accept,
+                 parent_idx, max_depth, temperature, top_p, top_k, seed, offset, rng_b0, u_accept,
                  u_final, out_accept_len, out_tokens, out_path, out_alpha, out_status, out_near,
                  out_final_dist};
   if (nthreads <= 1 || B <= 1) {

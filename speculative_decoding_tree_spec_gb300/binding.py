@@ -1,0 +1,297 @@
+"""ctypes binding of the C ABI in include/spec_verify.h.
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+library.  torch supplies device memory (the caching allocator) and the current
+stream.  The library must have been built (``__graft_entry__.build()``); loading
+fails loudly otherwise -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libspecverify.so")
+_lock = threading.Lock()
+_lib = None
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+SPEC_FLAG_EXACT_SELECT = 1
+SPEC_TREE_OK = 0
+SPEC_ROW_NONFINITE = 1
+SPEC_TREE_INVALID = 2
+SPEC_PHASE_PREPARE = 1
+SPEC_PHASE_ROWS = 2
+SPEC_PHASE_WALK = 4
+SPEC_PHASE_ALL = 7
+SPEC_MAX_NODES = 4096
+SPEC_MAX_VOCAB = 1 << 21
+ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_UNSUPPORTED_DTYPE",
+          -3: "SPEC_ERR_MISALIGNED", -4: "SPEC_ERR_WORKSPACE", -5: "SPEC_ERR_CUDA",
+          -6: "SPEC_ERR_TOO_LARGE"}
+
+
+class SamplingParams(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32),
+                ("top_p", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class RowStats(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_float), ("status", ctypes.c_int32), ("s_f", ctypes.c_double),
+                ("cut_key", ctypes.c_uint32), ("cut_idx", ctypes.c_int32),
+                ("argmax", ctypes.c_int32), ("kept", ctypes.c_int32)]
+
+
+class Counters(ctypes.Structure):
+    _fields_ = [("dense_rows", ctypes.c_uint64), ("dense_bytes", ctypes.c_uint64),
+                ("walk_bytes", ctypes.c_uint64), ("residual_passes", ctypes.c_uint64),
+                ("final_draws", ctypes.c_uint64), ("fallback_rows", ctypes.c_uint64),
+                ("reserved", ctypes.c_uint64 * 2)]
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {ERRORS.get(code, code)} ({error_string(code)})")
+        self.code = code
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA verify library missing at {LIB_PATH}; run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.c_void_p
+            i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+            L.spec_verify_workspace_size.argtypes = [i32, i32, i32, ctypes.c_int]
+            L.spec_verify_workspace_size.restype = ctypes.c_size_t
+            L.spec_verify_tree.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i64, i64, P, P, i32,
+                                           SamplingParams, u64, u64, P, P, P, P, P, P, P,
+                                           ctypes.c_size_t, P]
+            L.spec_verify_tree.restype = ctypes.c_int
+            L.spec_verify_tree_phases.argtypes = [ctypes.c_uint32] + L.spec_verify_tree.argtypes
+            L.spec_verify_tree_phases.restype = ctypes.c_int
+            L.spec_filter_rows.argtypes = [P, ctypes.c_int, i32, i32, i64, SamplingParams, P, P]
+            L.spec_filter_rows.restype = ctypes.c_int
+            L.spec_philox_words.argtypes = [u64, u64, P, P, i32, P, P]
+            L.spec_philox_words.restype = ctypes.c_int
+            L.spec_error_string.argtypes = [ctypes.c_int]
+            L.spec_error_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return lib().spec_error_string(int(code)).decode()
+
+
+def params(temperature: float, top_k: int = 0, top_p: float = 1.0, flags: int = 0) -> SamplingParams:
+    return SamplingParams(float(temperature), int(top_k), float(top_p), int(flags))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def workspace_size(B: int, N: int, V: int, dtype=torch.bfloat16) -> int:
+    code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
+    return int(lib().spec_verify_workspace_size(B, N, V, code))
+
+
+def _row_layout(t: torch.Tensor, B: int, N: int, V: int, broadcast: bool):
+    """(row_pitch, batch_stride) in elements of a [B, N, V] tensor, or of an [N, V]
+    tensor shared by every tree (batch_stride 0)."""
+    if t.stride(-1) != 1:
+        raise ValueError("logits rows must be contiguous in the vocabulary dimension")
+    if broadcast:
+        if tuple(t.shape) != (N, V):
+            raise ValueError(f"broadcast logits must be [N, V] = [{N}, {V}]")
+        return t.stride(0), 0
+    if tuple(t.shape) != (B, N, V):
+        raise ValueError(f"logits must be [B, N, V] = [{B}, {N}, {V}]")
+    return t.stride(1), t.stride(0)
+
+
+def verify_tree(p: torch.Tensor, q, draft_tokens: torch.Tensor, parent_idx: torch.Tensor,
+                max_depth: int, temperature: float, top_k: int = 0, top_p: float = 1.0,
+                seed: int = 0, offset: int = 0, flags: int = 0, *, batch_broadcast: bool = False,
+                want_alpha: bool = True, want_counters: bool = False, workspace=None, out=None,
+                stream=None, phases: int = SPEC_PHASE_ALL):
+    """spec_verify_tree on device tensors.  Returns a dict of device tensors:
+    accept_len [B], tokens [B, D+1], path [B, D+1], status [B], alpha [B, N] (if
+    requested) and counters (a Counters struct, synchronised, if requested)."""
+    B, N = draft_tokens.shape
+    V = p.shape[-1]
+    dev = p.device
+    if draft_tokens.dtype != torch.int32 or parent_idx.dtype != torch.int32:
+        raise TypeError("draft_tokens and parent_idx must be int32")
+    if not (draft_tokens.is_contiguous() and parent_idx.is_contiguous()):
+        raise ValueError("draft_tokens and parent_idx must be contiguous")
+    dt = _dtype_code(p)
+    pitch, bstride = _row_layout(p, B, N, V, batch_broadcast)
+    if q is not None:
+        if q.dtype != p.dtype:
+            raise TypeError("p and q logits must share a dtype")
+        if _row_layout(q, B, N, V, batch_broadcast) != (pitch, bstride):
+            raise ValueError("p and q must share one layout")
+    W = max_depth + 1
+    if out is None:
+        out = {
+            "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+            "tokens": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "path": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+        if want_alpha:
+            out["alpha"] = torch.empty((B, N), dtype=torch.float32, device=dev)
+    ws_bytes = int(lib().spec_verify_workspace_size(B, N, V, dt))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    counters = torch.zeros(8, dtype=torch.int64, device=dev) if want_counters else None
+    rc = lib().spec_verify_tree_phases(
+        int(phases), p.data_ptr(), None if q is None else q.data_ptr(), dt, B, N, V, pitch, bstride,
+        draft_tokens.data_ptr(), parent_idx.data_ptr(), int(max_depth),
+        params(temperature, top_k, top_p, flags), int(seed) & (2**64 - 1),
+        int(offset) & (2**64 - 1), out["accept_len"].data_ptr(), out["tokens"].data_ptr(),
+        out["path"].data_ptr(), out["alpha"].data_ptr() if "alpha" in out else None,
+        out["status"].data_ptr(), None if counters is None else counters.data_ptr(),
+        workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_verify_tree")
+    if counters is not None:
+        c = counters.cpu().numpy().view("uint64")
+        out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
+                                    "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))
+    return out
+
+
+def verify_tree_host(p_host: torch.Tensor, q_host, tokens_host: torch.Tensor,
+                     parents_host: torch.Tensor, max_depth: int, temperature: float,
+                     top_k: int = 0, top_p: float = 1.0, seed: int = 0, offset: int = 0,
+                     device="cuda", staging=None, stream=None):
+    """End-to-end call on host (ideally pinned) tensors: copies the inputs to the
+    device, verifies, and copies accept_len / tokens / path back.  `staging` may
+    hold preallocated device buffers (keys p, q, tokens, parents, workspace, out)."""
+    st = staging if staging is not None else {}
+    def dev_like(name, t):
+        if name not in st:
+            st[name] = torch.empty(t.shape, dtype=t.dtype, device=device)
+        st[name].copy_(t, non_blocking=True)
+        return st[name]
+    p = dev_like("p", p_host)
+    q = None if q_host is None else dev_like("q", q_host)
+    tok = dev_like("tokens", tokens_host)
+    par = dev_like("parents", parents_host)
+    res = verify_tree(p, q, tok, par, max_depth, temperature, top_k, top_p, seed, offset,
+                      want_alpha=False, workspace=st.get("workspace"), out=st.get("out"),
+                      stream=stream)
+    st.setdefault("out", res)
+    host = {k: res[k].to("cpu", non_blocking=True) for k in ("accept_len", "tokens", "path")}
+    torch.cuda.current_stream().synchronize()
+    return host
+
+
+def filter_rows(logits: torch.Tensor, temperature: float, top_k: int = 0, top_p: float = 1.0,
+                flags: int = 0, stream=None):
+    """spec_filter_rows on a [R, V] device tensor.  Returns a dict of device tensors
+    m, status, s_f, cut_key (int64), cut_idx, argmax, kept."""
+    if logits.dim() != 2 or logits.stride(-1) != 1:
+        raise ValueError("logits must be [R, V] with contiguous rows")
+    R, V = logits.shape
+    stats = torch.empty((max(R, 1), 32), dtype=torch.uint8, device=logits.device)
+    rc = lib().spec_filter_rows(logits.data_ptr(), _dtype_code(logits), R, V, logits.stride(0),
+                                params(temperature, top_k, top_p, flags), stats.data_ptr(),
+                                _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_filter_rows")
+    stats = stats[:R]
+    i32 = stats.view(torch.int32)
+    return {
+        "m": stats.view(torch.float32)[:, 0],
+        "status": i32[:, 1],
+        "s_f": stats.view(torch.float64)[:, 1],
+        "cut_key": i32[:, 4].to(torch.int64) & 0xFFFFFFFF,
+        "cut_idx": i32[:, 5],
+        "argmax": i32[:, 6],
+        "kept": i32[:, 7],
+    }
+
+
+def philox_words(seed: int, offset: int, b_idx: torch.Tensor, node_idx: torch.Tensor, stream=None):
+    """[n, 4] int64 tensor of the Philox words for (seed, offset, b_idx[i], node_idx[i])."""
+    n = b_idx.numel()
+    out = torch.empty((max(n, 1), 4), dtype=torch.int32, device=b_idx.device)
+    rc = lib().spec_philox_words(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                 b_idx.data_ptr(), node_idx.data_ptr(), n, out.data_ptr(),
+                                 _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_philox_words")
+    return out[:n].to(torch.int64) & 0xFFFFFFFF
+
+
+class PreparedVerify:
+    """A spec_verify_tree_phases call with every argument fixed (device tensors
+    allocated once), for loops that call the same verify step many times."""
+
+    def __init__(self, p, q, draft_tokens, parent_idx, max_depth, temperature, top_k=0,
+                 top_p=1.0, seed=0, offset=0, flags=0, batch_broadcast=False, stream=None):
+        B, N = draft_tokens.shape
+        V = p.shape[-1]
+        dev = p.device
+        dt = _dtype_code(p)
+        pitch, bstride = _row_layout(p, B, N, V, batch_broadcast)
+        if q is not None and _row_layout(q, B, N, V, batch_broadcast) != (pitch, bstride):
+            raise ValueError("p and q must share one layout")
+        W = max_depth + 1
+        self.out = {
+            "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+            "tokens": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "path": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+        self.counters = torch.zeros(8, dtype=torch.int64, device=dev)
+        ws_bytes = int(lib().spec_verify_workspace_size(B, N, V, dt))
+        self.workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self._keep = (p, q, draft_tokens, parent_idx)
+        self._fn = lib().spec_verify_tree_phases
+        self._args = [
+            p.data_ptr(), None if q is None else q.data_ptr(), dt, B, N, V, pitch, bstride,
+            draft_tokens.data_ptr(), parent_idx.data_ptr(), int(max_depth),
+            params(temperature, top_k, top_p, flags), int(seed) & (2**64 - 1),
+            int(offset) & (2**64 - 1), self.out["accept_len"].data_ptr(),
+            self.out["tokens"].data_ptr(), self.out["path"].data_ptr(), None,
+            self.out["status"].data_ptr(), None, self.workspace.data_ptr(),
+            self.workspace.numel(), _stream_ptr(stream)]
+        self._counter_args = list(self._args)
+        self._counter_args[19] = self.counters.data_ptr()
+
+    def __call__(self, phases: int = SPEC_PHASE_ALL) -> None:
+        rc = self._fn(phases, *self._args)
+        if rc != 0:
+            raise SpecError(rc, "spec_verify_tree_phases")
+
+    def read_counters(self) -> dict:
+        """Run the whole step once more with the work counters requested; returns them."""
+        rc = self._fn(SPEC_PHASE_ALL, *self._counter_args)
+        if rc != 0:
+            raise SpecError(rc, "spec_verify_tree_phases")
+        c = self.counters.cpu().numpy().view("uint64")
+        return dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
+                         "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))

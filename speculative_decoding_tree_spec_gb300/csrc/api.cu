@@ -1,0 +1,230 @@
+// api.cu -- the extern "C" entry points: host-side argument checks, workspace
+// carving and the three launches of one verify call (tree preparation, dense row
+// pass, tree walk) on the caller's stream.
+#include <cmath>
+
+#include "internal.h"
+
+namespace svk {
+
+int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+namespace {
+
+int elem_bytes(spec_dtype dt) { return dt == SPEC_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_params(const spec_sampling_params& prm) {
+  if (!std::isfinite(prm.temperature) || prm.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
+  if (!(prm.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also rejects NaN
+  if (prm.flags & ~SPEC_FLAG_EXACT_SELECT) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+int check_layout(const void* base, spec_dtype dt, int64_t row_pitch, int64_t batch_stride,
+                 int32_t V) {
+  if (row_pitch < V || batch_stride < 0) return SPEC_ERR_INVALID_ARG;
+  const int64_t s = elem_bytes(dt);
+  if (!aligned16(base) || (row_pitch * s) % 16 != 0 || (batch_stride * s) % 16 != 0)
+    return SPEC_ERR_MISALIGNED;
+  return SPEC_OK;
+}
+
+RowJob make_row_job(spec_dtype, int32_t V, const spec_sampling_params& prm) {
+  RowJob j{};
+  j.V = V;
+  j.temperature = prm.temperature;
+  j.c = prm.temperature > 0.0f ? (float)(1.4426950408889634 / (double)prm.temperature) : 0.0f;
+  j.delta_z = kWindowNats * prm.temperature;
+  j.top_k = (prm.top_k > 0 && prm.top_k < V) ? prm.top_k : 0;
+  j.top_p = prm.top_p >= 1.0f ? 1.0f : prm.top_p;
+  j.flags = prm.flags;
+  return j;
+}
+
+}  // namespace
+}  // namespace svk
+
+using namespace svk;
+
+extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t N, int32_t V, spec_dtype dtype) {
+  if (B < 0 || N < 1 || V < 1 || N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB) return 0;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return 0;
+  return ws_layout(B > 0 ? B : 1, N).total;
+}
+
+extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
+                                       const void* logits_q, spec_dtype dtype, int32_t B,
+                                       int32_t N, int32_t V, int64_t row_pitch,
+                                       int64_t batch_stride, const int32_t* draft_tokens,
+                                       const int32_t* parent_idx, int32_t max_depth,
+                                       spec_sampling_params params, uint64_t rng_seed,
+                                       uint64_t rng_offset, int32_t* out_accept_len,
+                                       int32_t* out_tokens, int32_t* out_accepted_path,
+                                       float* out_alpha, int32_t* out_status,
+                                       spec_verify_counters* out_counters, void* workspace,
+                                       size_t workspace_bytes, spec_stream_t stream) {
+  if (phases == 0 || (phases & ~SPEC_PHASE_ALL)) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || N < 1 || V < 1 || max_depth < 0) return SPEC_ERR_INVALID_ARG;
+  if (N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || max_depth >= SPEC_MAX_NODES)
+    return SPEC_ERR_TOO_LARGE;
+  int rc = check_params(params);
+  if (rc != SPEC_OK) return rc;
+  const bool greedy = params.temperature == 0.0f;
+  if (!logits_p || (!greedy && !logits_q) || !draft_tokens || !parent_idx || !out_accept_len ||
+      !out_tokens || !out_accepted_path || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  rc = check_layout(logits_p, dtype, row_pitch, batch_stride, V);
+  if (rc != SPEC_OK) return rc;
+  if (!greedy) {
+    rc = check_layout(logits_q, dtype, row_pitch, batch_stride, V);
+    if (rc != SPEC_OK) return rc;
+  }
+  const WsLayout L = ws_layout(B > 0 ? B : 1, N);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  if (B == 0) return SPEC_OK;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  spec_row_stats* stats_p = reinterpret_cast<spec_row_stats*>(ws + L.stats_p);
+  spec_row_stats* stats_q = reinterpret_cast<spec_row_stats*>(ws + L.stats_q);
+  unsigned long long* counters = reinterpret_cast<unsigned long long*>(ws + L.counters);
+
+  TreeJob tj{};
+  tj.base_p = logits_p;
+  tj.base_q = logits_q;
+  tj.row_pitch = row_pitch;
+  tj.batch_stride = batch_stride;
+  tj.V = V;
+  tj.N = N;
+  tj.B = B;
+  tj.W = max_depth + 1;
+  tj.tokens = draft_tokens;
+  tj.parents = parent_idx;
+  tj.child_start = reinterpret_cast<int32_t*>(ws + L.child_start);
+  tj.child_list = reinterpret_cast<int32_t*>(ws + L.child_list);
+  tj.need_q = reinterpret_cast<uint8_t*>(ws + L.need_q);
+  tj.tree_info = reinterpret_cast<int32_t*>(ws + L.tree_info);
+  tj.stats_p = stats_p;
+  tj.stats_q = stats_q;
+  tj.resid_z = reinterpret_cast<double*>(ws + L.resid_z);
+  tj.resid_invz = reinterpret_cast<float*>(ws + L.resid_invz);
+  tj.temperature = params.temperature;
+  tj.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)params.temperature);
+  tj.seed = rng_seed;
+  tj.offset = rng_offset;
+  tj.out_accept_len = out_accept_len;
+  tj.out_tokens = out_tokens;
+  tj.out_path = out_accepted_path;
+  tj.out_alpha = out_alpha;
+  tj.out_status = out_status;
+  tj.counters = counters;
+
+  if ((phases & SPEC_PHASE_PREPARE) && launch_tree_prep(tj, greedy, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  RowJob rj = make_row_job(dtype, V, params);
+  rj.base_p = logits_p;
+  rj.base_q = logits_q;
+  rj.row_pitch = row_pitch;
+  rj.batch_stride = batch_stride;
+  rj.N = N;
+  rj.B = B;
+  rj.mode = kRowsTree;
+  rj.with_q = greedy ? 0 : 1;
+  rj.need_q = tj.need_q;
+  rj.stats_p = stats_p;
+  rj.stats_q = stats_q;
+  rj.counters = counters;
+  const int virtual_rows = B * N * (greedy ? 1 : 2);
+  if ((phases & SPEC_PHASE_ROWS) && launch_row_pass(rj, dtype, virtual_rows, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  if (phases & SPEC_PHASE_WALK) {
+    if (launch_tree_walk(tj, dtype, greedy, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (out_counters &&
+        cudaMemcpyAsync(out_counters, counters, sizeof(spec_verify_counters),
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtype,
+                                int32_t B, int32_t N, int32_t V, int64_t row_pitch,
+                                int64_t batch_stride, const int32_t* draft_tokens,
+                                const int32_t* parent_idx, int32_t max_depth,
+                                spec_sampling_params params, uint64_t rng_seed,
+                                uint64_t rng_offset, int32_t* out_accept_len,
+                                int32_t* out_tokens, int32_t* out_accepted_path,
+                                float* out_alpha, int32_t* out_status,
+                                spec_verify_counters* out_counters, void* workspace,
+                                size_t workspace_bytes, spec_stream_t stream) {
+  return spec_verify_tree_phases(SPEC_PHASE_ALL, logits_p, logits_q, dtype, B, N, V, row_pitch,
+                                 batch_stride, draft_tokens, parent_idx, max_depth, params,
+                                 rng_seed, rng_offset, out_accept_len, out_tokens,
+                                 out_accepted_path, out_alpha, out_status, out_counters,
+                                 workspace, workspace_bytes, stream);
+}
+
+extern "C" int spec_filter_rows(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
+                                int64_t row_pitch, spec_sampling_params params,
+                                spec_row_stats* out_stats, spec_stream_t stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
+  if (R < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (V > SPEC_MAX_VOCAB) return SPEC_ERR_TOO_LARGE;
+  int rc = check_params(params);
+  if (rc != SPEC_OK) return rc;
+  if (!logits || !out_stats) return SPEC_ERR_INVALID_ARG;
+  rc = check_layout(logits, dtype, row_pitch, 0, V);
+  if (rc != SPEC_OK) return rc;
+  if (R == 0) return SPEC_OK;
+  RowJob rj = make_row_job(dtype, V, params);
+  rj.base_p = logits;
+  rj.row_pitch = row_pitch;
+  rj.R = R;
+  rj.mode = kRowsList;
+  rj.stats_p = out_stats;
+  if (launch_row_pass(rj, dtype, R, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+extern "C" int spec_philox_words(uint64_t seed, uint64_t offset, const int32_t* b_idx,
+                                 const int32_t* node_idx, int32_t n, uint32_t* out_words,
+                                 spec_stream_t stream) {
+  if (n < 0) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  if (!b_idx || !node_idx || !out_words) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(out_words)) return SPEC_ERR_MISALIGNED;
+  if (launch_philox_words(seed, offset, b_idx, node_idx, n, out_words,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+extern "C" const char* spec_error_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "success";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case SPEC_ERR_MISALIGNED: return "misaligned pointer or stride (16-byte alignment required)";
+    case SPEC_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case SPEC_ERR_CUDA: return "CUDA launch failed";
+    case SPEC_ERR_TOO_LARGE: return "size above the library limits";
+    default: return "unknown error code";
+  }
+}

@@ -137,8 +137,24 @@ def _torch_dtype(w: Workload):
     return torch.float32 if w.dtype == "f32" else torch.bfloat16
 
 
+def padded_pitch(V: int, elem_bytes: int) -> int:
+    """Row pitch (elements) of a 16-byte aligned row of V elements."""
+    per = 16 // elem_bytes
+    return (V + per - 1) // per * per
+
+
+def empty_rows(shape, dtype, device):
+    """An uninitialised [..., V] tensor whose rows start on 16-byte boundaries (a view
+    into a buffer padded to an aligned row pitch)."""
+    V = shape[-1]
+    Vp = padded_pitch(V, torch.tensor([], dtype=dtype).element_size())
+    buf = torch.empty(tuple(shape[:-1]) + (Vp,), dtype=dtype, device=device)
+    return buf[..., :V]
+
+
 def make_logits(w: Workload, seed: int, device="cpu", chunk_rows: int = 512):
-    """Target and draft logits, each [B, N, V] in the workload's dtype.
+    """Target and draft logits, each [B, N, V] in the workload's dtype (rows on
+    16-byte boundaries: a padded row pitch when V * elem_bytes is not a multiple of 16).
 
     gauss: target z ~ N(0, sigma^2) i.i.d.; draft = z + N(0, draft_noise^2).
     zipf:  bias(v) = -1.1 ln(rank(v)), rank from a per-row affine permutation
@@ -149,10 +165,10 @@ def make_logits(w: Workload, seed: int, device="cpu", chunk_rows: int = 512):
     g.manual_seed(int(seed))
     B, N, V = w.B, w.N, w.V
     dt = _torch_dtype(w)
-    p = torch.empty((B, N, V), dtype=dt, device=device)
-    q = torch.empty((B, N, V), dtype=dt, device=device)
-    pf = p.view(B * N, V)
-    qf = q.view(B * N, V)
+    p = empty_rows((B, N, V), dt, device)
+    q = empty_rows((B, N, V), dt, device)
+    pf = p.as_strided((B * N, V), (p.stride(1), 1))   # row view over all B*N rows
+    qf = q.as_strided((B * N, V), (q.stride(1), 1))
     rows = B * N
     if w.logits == "zipf":
         rng = np.random.default_rng(seed + 7919)

@@ -1,0 +1,317 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Token ids, accepted lengths, paths, argmax and cut indices
+must match exactly; probabilities within 1e-5 relative for fp32 logits and 2e-3
+for bf16 logits.  Trees / rows the oracle flags as within 1e-6 of a decision
+boundary are excluded from the exact comparison and counted."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_helpers import compare, gpu_inputs, run_gpu, run_oracle
+from speculative_decoding_tree_spec_gb300 import binding
+from speculative_decoding_tree_spec_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+W = wl.WORKLOADS
+
+
+# --- Philox ----------------------------------------------------------------------
+
+def test_philox_words_match_oracle():
+    rng = np.random.default_rng(0)
+    n = 4096
+    b = rng.integers(0, 2**31 - 1, size=n).astype(np.int32)
+    node = rng.integers(0, 5000, size=n).astype(np.int32)
+    for seed, offset in ((0, 0), (0xDEADBEEFCAFEF00D, 0), (12345, (7 << 32) | 99)):
+        g = binding.philox_words(seed, offset, torch.as_tensor(b, device=DEV),
+                                 torch.as_tensor(node, device=DEV)).cpu().numpy()
+        for i in range(0, n, 97):
+            ctr = [node[i], b[i], offset & 0xFFFFFFFF, offset >> 32]
+            key = [seed & 0xFFFFFFFF, seed >> 32]
+            assert list(g[i]) == list(oracle.philox4x32_10(ctr, key)), i
+
+
+# --- the dense row pass ----------------------------------------------------------
+
+def _rows(kind, R, V, dtype, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    if kind == "gauss":
+        x = torch.randn((R, V), generator=g) * 3
+    elif kind == "ties":
+        x = torch.randint(-6, 7, (R, V), generator=g).float() * 0.5
+    elif kind == "flat":
+        x = torch.randn((R, V), generator=g) * 0.05
+    elif kind == "zipf":
+        rank = torch.stack([torch.randperm(V, generator=g) for _ in range(R)]).float() + 1
+        x = -1.1 * torch.log(rank) + torch.randn((R, V), generator=g) * 2
+    elif kind == "masked":
+        x = torch.randn((R, V), generator=g) * 3
+        x[torch.rand((R, V), generator=g) < 0.7] = float("-inf")
+        x[:, 0] = 0.0
+    else:
+        raise ValueError(kind)
+    return x.to(dtype)
+
+
+def _dev_rows(x):
+    """Device copy of [R, V] rows with a 16-byte aligned row pitch."""
+    d = wl.empty_rows(tuple(x.shape), x.dtype, DEV)
+    d.copy_(x)
+    return d
+
+
+def _check_rows(x, T, k, p, flags=0):
+    st = binding.filter_rows(_dev_rows(x), T, k, p, flags)
+    torch.cuda.synchronize()
+    st = {a: b.cpu().numpy() for a, b in st.items()}
+    host = x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 else x.numpy()
+    _, infos = oracle.filter_rows(host, T, k, p)
+    rtol = 2e-3 if x.dtype == torch.bfloat16 else 1e-5
+    worst = 0.0
+    near = 0
+    for r, info in enumerate(infos):
+        assert st["status"][r] == info.status, r
+        if info.status:
+            continue
+        assert st["argmax"][r] == info.argmax, r
+        assert st["m"][r] == np.float32(info.m), r
+        if info.near:
+            near += 1
+            continue
+        V = x.shape[1]
+        if T > 0 and not (0 < k < V) and p >= 1:
+            # nothing truncated: the row reports the "every token passes" cut
+            assert (st["cut_key"][r], st["cut_idx"][r], st["kept"][r]) == (0, V - 1, V)
+            assert info.kept == V
+        else:
+            assert st["cut_idx"][r] == info.cut_idx, (r, st["cut_idx"][r], info.cut_idx)
+        assert st["kept"][r] == info.kept, (r, st["kept"][r], info.kept)
+        rel = abs(st["s_f"][r] - info.s_f) / info.s_f
+        worst = max(worst, rel)
+        assert rel <= rtol, (r, st["s_f"][r], info.s_f)
+    return st, worst, near
+
+
+PARAMS = [(0.0, 0, 1.0), (1.0, 0, 1.0), (0.7, 0, 0.9), (1.0, 50, 0.95), (0.5, 5, 1.0),
+          (2.0, 0, 0.5), (1.0, 1, 1.0), (0.8, 0, 0.999), (1.3, 300, 0.8)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("kind", ["gauss", "ties", "flat", "zipf", "masked"])
+@pytest.mark.parametrize("V", [1, 7, 33, 1000, 32000])
+def test_filter_rows_match_oracle(dtype, kind, V):
+    x = _rows(kind, 6, V, dtype, seed=V * 31 + len(kind))
+    for T, k, p in PARAMS:
+        st, worst, near = _check_rows(x, T, k, p)
+        if T > 0 and (p < 1 or 0 < k < V):
+            st2 = binding.filter_rows(_dev_rows(x), T, k, p, binding.SPEC_FLAG_EXACT_SELECT)
+            torch.cuda.synchronize()
+            for key in ("cut_idx", "kept", "s_f", "cut_key", "argmax", "m"):
+                np.testing.assert_array_equal(st[key], st2[key].cpu().numpy(), err_msg=key)
+
+
+@pytest.mark.parametrize("V", [128256, 152064])
+def test_filter_rows_large_vocab(V):
+    for kind, (T, k, p) in (("gauss", (0.7, 0, 0.9)), ("zipf", (1.0, 50, 0.95)),
+                            ("flat", (1.0, 0, 0.9)), ("ties", (1.0, 0, 0.95))):
+        x = _rows(kind, 4, V, torch.bfloat16, seed=V + k)
+        st, worst, near = _check_rows(x, T, k, p)
+        st2 = binding.filter_rows(_dev_rows(x), T, k, p, binding.SPEC_FLAG_EXACT_SELECT)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(st["cut_idx"], st2["cut_idx"].cpu().numpy())
+        np.testing.assert_array_equal(st["s_f"], st2["s_f"].cpu().numpy())
+
+
+def test_filter_rows_non_finite():
+    x = torch.randn((5, 100)) * 2
+    x[0, 3] = float("nan")
+    x[1, 50] = float("inf")
+    x[2, :] = float("-inf")
+    x[3, :90] = float("-inf")
+    for T, k, p in ((0.0, 0, 1.0), (1.0, 0, 1.0), (1.0, 0, 0.9), (1.0, 20, 1.0)):
+        st = binding.filter_rows(_dev_rows(x), T, k, p)
+        torch.cuda.synchronize()
+        s = st["status"].cpu().numpy()
+        assert list(s) == [1, 1, 1, 0, 0], (T, k, p, s)
+
+
+def test_filter_rows_negative_zero_ties():
+    x = torch.tensor([[-0.0, 0.0, -1.0, -0.0, -3.0]])
+    st = binding.filter_rows(_dev_rows(x), 1.0, 2, 1.0)
+    torch.cuda.synchronize()
+    assert st["argmax"].item() == 0 and st["cut_idx"].item() == 1
+
+
+# --- the full verify step ----------------------------------------------------------
+
+def _parity(w, seed, trees=None, **kw):
+    inp = gpu_inputs(w, seed)
+    gpu = run_gpu(w, inp, seed=seed + 1, **kw)
+    sel, outs = run_oracle(w, inp, trees=trees, seed=seed + 1, **{k: v for k, v in kw.items()
+                                                                if k != "flags"})
+    n, ex, err = compare(w, gpu, sel, outs)
+    assert n >= max(1, len(sel) // 2), f"too many excluded trees: {ex} of {len(sel)}"
+    return gpu, n, ex, err
+
+
+def test_chain_v32_full():
+    w = W["chain_g3_v32"]
+    gpu, n, ex, err = _parity(w, seed=3)
+    assert n > 9900
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_eagle10_v32000(T):
+    w = W["eagle10_v32000"].with_(B=24, temperature=T)
+    _parity(w, seed=11)
+
+
+@pytest.mark.parametrize("w", [
+    W["tree60_b64_v128256"].with_(B=6),
+    W["tree26_b256_v152064"].with_(B=6),
+    W["tree60_b64_v128256"].with_(B=6, dtype="f32", V=32000),
+    W["tree26_b256_v152064"].with_(B=6, temperature=0.0),
+    W["tree60_b64_v128256"].with_(B=8, N=40, V=5003, temperature=1.3, top_k=7, top_p=0.8),
+    W["tree60_b64_v128256"].with_(B=8, N=33, V=999, dtype="f32", temperature=0.9, top_k=0,
+                                  top_p=1.0),
+], ids=["c3-reduced", "c4-reduced", "c3-f32", "c4-greedy", "ragged-topk-topp", "f32-plain"])
+def test_random_trees(w):
+    _parity(w, seed=21)
+
+
+def test_exact_select_flag_gives_identical_outputs():
+    w = W["tree60_b64_v128256"].with_(B=6, V=40000)
+    inp = gpu_inputs(w, 5)
+    a = run_gpu(w, inp, seed=9)
+    b = run_gpu(w, inp, seed=9, flags=binding.SPEC_FLAG_EXACT_SELECT)
+    for key in ("accept_len", "tokens", "path", "status"):
+        np.testing.assert_array_equal(a[key], b[key])
+    np.testing.assert_array_equal(a["alpha"], b["alpha"])
+    assert b["counters"]["fallback_rows"] == b["counters"]["dense_rows"]
+
+
+def test_top1_sampling_equals_greedy_on_gpu():
+    w = W["tree26_b256_v152064"].with_(B=8, V=20000)
+    inp = gpu_inputs(w, 8)
+    g = run_gpu(w, inp, temperature=0.0, top_k=0, top_p=1.0)
+    s = run_gpu(w, inp, temperature=0.9, top_k=1, top_p=1.0)
+    np.testing.assert_array_equal(g["accept_len"], s["accept_len"])
+    np.testing.assert_array_equal(g["tokens"], s["tokens"])
+
+
+def test_repeat_calls_are_bit_identical():
+    w = W["tree60_b64_v128256"].with_(B=8, V=50000)
+    inp = gpu_inputs(w, 4)
+    a = run_gpu(w, inp, seed=3, offset=10)
+    b = run_gpu(w, inp, seed=3, offset=10)
+    c = run_gpu(w, inp, seed=3, offset=11)
+    for key in ("accept_len", "tokens", "path", "alpha"):
+        np.testing.assert_array_equal(a[key], b[key])
+    assert not np.array_equal(a["tokens"], c["tokens"]) or not np.array_equal(a["alpha"], c["alpha"])
+
+
+# --- edge cases --------------------------------------------------------------------
+
+def _manual(p, q, tokens, parents, D, T, k=0, top_p=1.0, seed=1, broadcast=False):
+    pd = _dev_rows(torch.as_tensor(p))
+    qd = _dev_rows(torch.as_tensor(q))
+    out = binding.verify_tree(pd, qd, torch.as_tensor(tokens, device=DEV),
+                              torch.as_tensor(parents, device=DEV), D, T, k, top_p, seed=seed,
+                              batch_broadcast=broadcast)
+    torch.cuda.synchronize()
+    gpu = {a: b.cpu().numpy() for a, b in out.items()}
+    ref = oracle.verify_tree(np.asarray(p), np.asarray(q), tokens, parents, D, T, k, top_p,
+                             seed=seed, batch_broadcast=broadcast)
+    return gpu, ref
+
+
+def _assert_same(gpu, ref):
+    keep = ref["near"] == 0
+    np.testing.assert_array_equal(gpu["status"], ref["status"])
+    np.testing.assert_array_equal(gpu["accept_len"][keep], ref["accept_len"][keep])
+    np.testing.assert_array_equal(gpu["tokens"][keep], ref["tokens"][keep])
+    np.testing.assert_array_equal(gpu["path"][keep], ref["path"][keep])
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_root_only_and_single_token_vocab(T):
+    rng = np.random.default_rng(1)
+    p = rng.normal(size=(50, 1, 77)).astype(np.float32)
+    gpu, ref = _manual(p, p, np.zeros((50, 1), np.int32), np.full((50, 1), -1, np.int32), 0, T)
+    _assert_same(gpu, ref)
+    p1 = rng.normal(size=(5, 3, 1)).astype(np.float32)
+    par = np.tile(np.array([-1, 0, 1], np.int32), (5, 1))
+    gpu, ref = _manual(p1, p1, np.zeros((5, 3), np.int32), par, 2, T)
+    _assert_same(gpu, ref)
+    assert (gpu["accept_len"] == 2).all()
+
+
+def test_invalid_trees_and_nonfinite_rows():
+    rng = np.random.default_rng(2)
+    B, N, V = 6, 5, 40
+    p = rng.normal(size=(B, N, V)).astype(np.float32)
+    q = rng.normal(size=(B, N, V)).astype(np.float32)
+    par = np.tile(np.array([-1, 0, 0, 1, 3], np.int32), (B, 1))
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    par[1, 0] = 0          # root must be -1
+    par[2, 3] = 4          # parent after child
+    tok[3, 2] = V          # token out of range
+    p[4, 0, 5] = np.nan    # non-finite root row
+    gpu, ref = _manual(p, q, tok, par, 3, 1.0)
+    assert list(gpu["status"][:5]) == [0, 2, 2, 2, 1]
+    _assert_same(gpu, ref)
+    gpu, ref = _manual(p, q, tok, par, 2, 1.0)   # depth 3 > max_depth 2: all invalid
+    assert (gpu["status"] == 2).all() and (gpu["accept_len"] == -1).all()
+
+
+def test_broadcast_rows_and_deep_chain():
+    rng = np.random.default_rng(3)
+    N, V, B = 300, 64, 40
+    p = rng.normal(0, 0.3, size=(N, V)).astype(np.float32)
+    q = (p + rng.normal(0, 0.05, size=(N, V))).astype(np.float32)
+    par = np.tile(wl.chain_tree(N), (B, 1))
+    tok = np.zeros((B, N), np.int32)
+    tok[:, 1:] = rng.integers(0, V, size=(B, N - 1))
+    gpu, ref = _manual(p, q, tok, par, N - 1, 1.0, broadcast=True)
+    _assert_same(gpu, ref)
+
+
+def test_max_nodes_tree():
+    rng = np.random.default_rng(4)
+    N, V, B = binding.SPEC_MAX_NODES, 16, 2
+    par = np.stack([wl.random_tree(N, 12, 4, rng) for _ in range(B)])
+    p = rng.normal(size=(B, N, V)).astype(np.float32)
+    q = rng.normal(size=(B, N, V)).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    for T in (0.0, 1.0):
+        gpu, ref = _manual(p, q, tok, par, 12, T)
+        _assert_same(gpu, ref)
+
+
+def test_chi_squared_first_token_on_gpu():
+    """1e6 trees sharing one set of rows: the first emitted token follows filt(p_root)
+    when the siblings are drawn i.i.d. from filt(q_root)."""
+    from scipy import stats
+    rng = np.random.default_rng(5)
+    V, T, k, tp = 8, 0.9, 6, 0.95
+    parents = np.array([-1, 0, 0, 0, 1, 1, 2], np.int32)
+    N = len(parents)
+    p = rng.normal(0, 1.0, size=(N, V)).astype(np.float32)
+    q = (p + rng.normal(0, 0.8, size=(N, V))).astype(np.float32)
+    B = 1_000_000
+    Qs = [oracle.filter_row(q[u], T, k, tp)[0] for u in range(N)]
+    tok = np.zeros((B, N), np.int32)
+    for c in range(1, N):
+        tok[:, c] = rng.choice(V, size=B, p=Qs[parents[c]])
+    out = binding.verify_tree(_dev_rows(torch.as_tensor(p)), _dev_rows(torch.as_tensor(q)),
+                              torch.as_tensor(tok, device=DEV),
+                              torch.as_tensor(np.tile(parents, (B, 1)), device=DEV), 2, T, k, tp,
+                              seed=2024, batch_broadcast=True, want_alpha=False)
+    first = out["tokens"][:, 0].cpu().numpy()
+    P0 = oracle.filter_row(p[0], T, k, tp)[0]
+    obs = np.bincount(first, minlength=V)
+    m = P0 > 0
+    assert obs[~m].sum() == 0
+    assert stats.chisquare(obs[m], P0[m] * B).pvalue > 1e-3

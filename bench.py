@@ -349,7 +349,7 @@ def run_ours(args):
         "step_hbm_gbs": (counters["dense_bytes"] + counters["walk_bytes"]) / (ms_per_step / 1e3) / 1e9,
         "work_per_step": counters,
         "roofline": roofline,
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,  # row_pass_kernel + tree_walk_kernel per step
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
 

@@ -65,6 +65,11 @@ typedef struct {
 /* Select the top-k / top-p cut with the full-row radix selection even where the
  * single-pass candidate window would do (both give identical results). */
 #define SPEC_FLAG_EXACT_SELECT 1u
+/* Self-test of the device-side wait limits (for tests only): the dense row pass
+ * withholds the completion of one of its shared-memory copies, so that the bounded
+ * wait on it expires (after 20 ms); the affected rows report SPEC_ROW_TIMEOUT and
+ * the call still completes. */
+#define SPEC_FLAG_TEST_STALL 2u
 
 /* Return codes. */
 #define SPEC_OK 0
@@ -79,6 +84,8 @@ typedef struct {
 #define SPEC_TREE_OK 0
 #define SPEC_ROW_NONFINITE 1 /* a row the walk needed holds NaN or +inf, or is all -inf */
 #define SPEC_TREE_INVALID 2  /* parent_idx / draft_tokens malformed, or depth > max_depth */
+#define SPEC_ROW_TIMEOUT 3   /* a bounded device-side wait gave up: the row's statistics are
+                                not valid (see SPEC_FLAG_TEST_STALL) */
 
 /* Size limits checked on the host. */
 #define SPEC_MAX_NODES 4096
@@ -93,7 +100,7 @@ typedef struct {
  * the row reports cut_key = 0, cut_idx = V - 1, kept = V. */
 typedef struct {
   float m;          /* maximum logit of the row */
-  int32_t status;   /* SPEC_TREE_OK or SPEC_ROW_NONFINITE */
+  int32_t status;   /* SPEC_TREE_OK, SPEC_ROW_NONFINITE or SPEC_ROW_TIMEOUT */
   double s_f;       /* sum over kept tokens of exp((z - m) / T); 1 at T == 0 */
   uint32_t cut_key; /* key of the last kept token in rank order */
   int32_t cut_idx;  /* vocabulary index of that token */
@@ -136,7 +143,8 @@ size_t spec_verify_workspace_size(int32_t B, int32_t N, int32_t V, spec_dtype dt
  *   out_accepted_path [B, W]: node 0, then the accepted nodes, then -1 padding;
  *   out_alpha [B, N] (optional, may be NULL): the acceptance probability used for
  *     every tested node, NaN for untested nodes (greedy: 1 accept, 0 reject);
- *   out_status [B] (optional): SPEC_TREE_OK / SPEC_ROW_NONFINITE / SPEC_TREE_INVALID;
+ *   out_status [B] (optional): SPEC_TREE_OK / SPEC_ROW_NONFINITE / SPEC_TREE_INVALID /
+ *     SPEC_ROW_TIMEOUT;
  *   out_counters (optional): work counters of this call.
  * workspace: device scratch of at least spec_verify_workspace_size() bytes,
  *   256-byte aligned; its contents are not preserved between calls.
@@ -155,9 +163,11 @@ int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtyp
                      void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /* Phases of one verify call, for spec_verify_tree_phases. */
-#define SPEC_PHASE_PREPARE 1u /* validate the trees, build child lists, mark needed q rows */
-#define SPEC_PHASE_ROWS 2u    /* dense row pass: row statistics of every p and needed q row */
-#define SPEC_PHASE_WALK 4u    /* the accept walk, residual renormalisation and final draw */
+#define SPEC_PHASE_PREPARE 1u /* reset the work counters (when out_counters is requested) */
+#define SPEC_PHASE_ROWS 2u    /* dense row pass: statistics of every p row and of the q row
+                                 of every node that has a child */
+#define SPEC_PHASE_WALK 4u    /* tree checks, the accept walk, residual renormalisation and
+                                 the final draw */
 #define SPEC_PHASE_ALL 7u
 
 /*

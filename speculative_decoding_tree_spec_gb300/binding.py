@@ -21,9 +21,11 @@ _lib = None
 SPEC_F32 = 0
 SPEC_BF16 = 1
 SPEC_FLAG_EXACT_SELECT = 1
+SPEC_FLAG_TEST_STALL = 2
 SPEC_TREE_OK = 0
 SPEC_ROW_NONFINITE = 1
 SPEC_TREE_INVALID = 2
+SPEC_ROW_TIMEOUT = 3
 SPEC_PHASE_PREPARE = 1
 SPEC_PHASE_ROWS = 2
 SPEC_PHASE_WALK = 4

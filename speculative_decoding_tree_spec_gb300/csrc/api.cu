@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points: host-side argument checks, workspace
-// carving and the three launches of one verify call (tree preparation, dense row
-// pass, tree walk) on the caller's stream.
+// carving and the launches of one verify call on the caller's stream: (prepare)
+// zero the work counters when they are requested, (rows) the dense row pass,
+// (walk) the per-tree accept walk.
 #include <cmath>
 
 #include "internal.h"
@@ -28,7 +29,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_params(const spec_sampling_params& prm) {
   if (!std::isfinite(prm.temperature) || prm.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
   if (!(prm.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also rejects NaN
-  if (prm.flags & ~SPEC_FLAG_EXACT_SELECT) return SPEC_ERR_INVALID_ARG;
+  if (prm.flags & ~(SPEC_FLAG_EXACT_SELECT | SPEC_FLAG_TEST_STALL)) return SPEC_ERR_INVALID_ARG;
   return SPEC_OK;
 }
 
@@ -50,6 +51,8 @@ RowJob make_row_job(spec_dtype, int32_t V, const spec_sampling_params& prm) {
   j.top_k = (prm.top_k > 0 && prm.top_k < V) ? prm.top_k : 0;
   j.top_p = prm.top_p >= 1.0f ? 1.0f : prm.top_p;
   j.flags = prm.flags;
+  // a healthy wait lasts microseconds; the stall self-test uses a short limit
+  j.wait_limit_ns = (prm.flags & SPEC_FLAG_TEST_STALL) ? 20000000ull : 2000000000ull;
   return j;
 }
 
@@ -114,14 +117,8 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   tj.W = max_depth + 1;
   tj.tokens = draft_tokens;
   tj.parents = parent_idx;
-  tj.child_start = reinterpret_cast<int32_t*>(ws + L.child_start);
-  tj.child_list = reinterpret_cast<int32_t*>(ws + L.child_list);
-  tj.need_q = reinterpret_cast<uint8_t*>(ws + L.need_q);
-  tj.tree_info = reinterpret_cast<int32_t*>(ws + L.tree_info);
   tj.stats_p = stats_p;
   tj.stats_q = stats_q;
-  tj.resid_z = reinterpret_cast<double*>(ws + L.resid_z);
-  tj.resid_invz = reinterpret_cast<float*>(ws + L.resid_invz);
   tj.temperature = params.temperature;
   tj.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)params.temperature);
   tj.seed = rng_seed;
@@ -131,9 +128,11 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   tj.out_path = out_accepted_path;
   tj.out_alpha = out_alpha;
   tj.out_status = out_status;
-  tj.counters = counters;
+  // work counters are kept only when the caller asks for them
+  tj.counters = out_counters ? counters : nullptr;
 
-  if ((phases & SPEC_PHASE_PREPARE) && launch_tree_prep(tj, greedy, s) != cudaSuccess)
+  if ((phases & SPEC_PHASE_PREPARE) && out_counters &&
+      cudaMemsetAsync(counters, 0, sizeof(spec_verify_counters), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   RowJob rj = make_row_job(dtype, V, params);
@@ -145,10 +144,10 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   rj.B = B;
   rj.mode = kRowsTree;
   rj.with_q = greedy ? 0 : 1;
-  rj.need_q = tj.need_q;
+  rj.parents = parent_idx;
   rj.stats_p = stats_p;
   rj.stats_q = stats_q;
-  rj.counters = counters;
+  rj.counters = tj.counters;
   const int virtual_rows = B * N * (greedy ? 1 : 2);
   if ((phases & SPEC_PHASE_ROWS) && launch_row_pass(rj, dtype, virtual_rows, s) != cudaSuccess)
     return SPEC_ERR_CUDA;

@@ -142,6 +142,11 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
   return v;
 }
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
 __device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -158,6 +163,121 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
+// Float-float (hi, lo) arithmetic: error-free two-sum in fp32.  Used instead of
+// per-thread fp64, whose throughput on this part is a small fraction of fp32.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+struct FF {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    float s, e;
+    two_sum(hi, x, s, e);
+    lo += e;
+    hi = s;
+  }
+  __device__ __forceinline__ void add(const FF& o) {
+    float s, e;
+    two_sum(hi, o.hi, s, e);
+    lo += e + o.lo;
+    hi = s;
+  }
+  __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
+};
+// Butterfly sum of a float-float value over the warp (every lane gets the total).
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    FF t;
+    t.hi = __shfl_xor_sync(kFull, v.hi, o);
+    t.lo = __shfl_xor_sync(kFull, v.lo, o);
+    v.add(t);
+  }
+  return v;
+}
+
+// 16-byte asynchronous global -> shared copies (each thread later reads only the
+// bytes it copied itself, so no block barrier is needed between stages).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// mbarriers and bulk (TMA) copies.  Every wait is bounded in time: once
+// `limit_ns` have passed (read from %globaltimer) it gives up and returns false,
+// and the caller records a timeout and carries on without waiting again, so no
+// wait -- and no barrier behind it -- can hold the GPU.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
+                   smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for the phase with `parity` to complete; false once limit_ns have passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+// Bulk global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) that signals `bar` with its byte count on completion.
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Named barrier over the first `nthreads` threads of the block (barrier id 1).
+__device__ __forceinline__ void named_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;\n" ::"r"(nthreads) : "memory");
+}
+
 // Kahan-compensated fp32 accumulator.
 struct Kahan {
   float s = 0.f, c = 0.f;
@@ -168,6 +288,11 @@ struct Kahan {
     s = t;
   }
   __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+  __device__ __forceinline__ FF ff() const {
+    FF r;
+    two_sum(s, -c, r.hi, r.lo);
+    return r;
+  }
 };
 
 }  // namespace svk

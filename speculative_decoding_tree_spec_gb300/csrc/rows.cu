@@ -3,20 +3,26 @@
 // EAGLE", section 1 note: p and q are compared after temperature, top-k, top-p or
 // argmax processing).
 //
-// One block of kRowThreads threads owns one row at a time (persistent grid-stride
-// over rows).  A single streaming pass over the row computes
+// One persistent block per SM, warp-specialised: one producer warp streams the
+// block's rows, chunk after chunk, into a ring of kRingStages shared-memory stages
+// with bulk (TMA) copies, running ahead across row boundaries; kRowThreads
+// consumer threads own one row at a time.  A single pass over each chunk computes
 //   * each warp's running maximum and the sum of 2^((z - M_warp) c), rescaled
 //     whenever the warp maximum grows (online softmax), Kahan-summed;
-//   * the argmax (lowest index of the maximum);
+//   * the maximum (its lowest index is recovered at the end of the row);
 //   * when top-k / top-p is active, a candidate window: every token within
-//     kWindowNats nats of the block's running maximum is appended to shared memory.
+//     kWindowNats nats of the block's running maximum is appended to its warp's
+//     region of shared memory.
 // The cut is then found inside the window.  bf16 windows are resolved with an
 // exact histogram over their (few hundred) distinct keys -- equal logits carry
 // equal weights, so a bin's mass is its count times one weight; fp32 windows are
 // sorted.  Masses are 42-bit fixed point, so every sum is exact and independent
 // of order.  When the window overflows or provably misses the cut, the row falls
 // back to an exact full-row selection by 4-way bisection on the order key; both
-// routes produce bit-identical statistics.
+// routes produce bit-identical statistics.  Consumer-only synchronisation uses a
+// named barrier, so the producer keeps streaming while a row is being selected.
+#include <cuda_bf16.h>
+
 #include <climits>
 
 #include "common.cuh"
@@ -25,13 +31,22 @@ namespace svk {
 
 namespace {
 
-constexpr int NT = kRowThreads;
-constexpr int NW = NT / 32;
-constexpr int kUnroll = 4;
-constexpr int kBinsPerThread = kHistBins / NT;
-constexpr size_t kDynSmem = (size_t)kCandCap * 8 + (size_t)kSortCap * 8;
+constexpr int NT = kRowThreads;        // consumer threads
+constexpr int NW = NT / 32;            // consumer warps
+constexpr int kBlockThreads = NT + 32; // + the producer warp
+constexpr int kStageBytes = kRingUnits * NT * 16;
+
+// barrier over the consumer threads only
+__device__ __forceinline__ void csync() { named_sync(NT); }
 
 struct RowShared {
+  unsigned wcnt[NW];     // candidates appended by each warp (may exceed its region)
+  int woverflow[NW];
+  int tmo;              // a bounded wait gave up in this block (sticky)
+  int sel_ok, sel_bcut;
+  unsigned sel_jcut, sel_kept, sel_ncut;
+  unsigned long long sel_sf;
+  uint32_t sel_cutkey;
   float warp_m[NW];
   double warp_s[NW];
   float warp_best[NW];
@@ -47,8 +62,8 @@ struct RowShared {
   unsigned tie_n;
   int tie_idx;
   unsigned sel_j;
-  unsigned red_cnt[4];
-  unsigned long long red_mass[4];
+  unsigned red_cnt[8];
+  unsigned long long red_mass[8];
   unsigned red_min;
   unsigned long long tau;
   // results broadcast by thread 0
@@ -57,6 +72,10 @@ struct RowShared {
   int argmax;
   int bad;
 };
+
+__device__ __forceinline__ __nv_bfloat162 bf2(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
 
 __device__ __forceinline__ const void* row_ptr(const void* base, int64_t elems, int bytes) {
   return static_cast<const void*>(static_cast<const char*>(base) + elems * bytes);
@@ -75,9 +94,9 @@ __device__ void block_exscan(unsigned c, unsigned long long w, unsigned& base_c,
     unsigned long long tw = __shfl_up_sync(kFull, iw, o);
     if (lane >= o) { ic += tc; iw += tw; }
   }
-  __syncthreads();
+  csync();
   if (lane == 31) { sh.warp_cnt[warp] = ic; sh.warp_mass[warp] = iw; }
-  __syncthreads();
+  csync();
   unsigned bc = 0, tc = 0;
   unsigned long long bw = 0, tw = 0;
   for (int i = 0; i < NW; ++i) {
@@ -114,16 +133,23 @@ struct SelOut {
   uint64_t mass_kept;     // their fixed-point mass
 };
 
-// Tallies of eligible tokens with (key >> ks) >= th[t], t < 3, plus the minimum
-// eligible shifted key.  Results land in sh.red_cnt / sh.red_mass / sh.red_min.
+// Tallies over eligible tokens whose shifted key s = key >> ks lies in [th[0], hi]:
+// for each t, the count and fixed-point mass of those with s >= th[t]; plus the
+// minimum eligible shifted key.  Weights are computed only inside the range.
+// Results land in sh.red_cnt / sh.red_mass / sh.red_min.
+constexpr int kSplit = 7;  // thresholds per pass: an 8-way split of the key range
+
 template <typename T>
-__device__ void tally3(const void* row, int V, float m, float c, int ks, const uint32_t (&th)[3],
-                       const Eligible& elig, RowShared& sh) {
+__device__ void tally_range(const void* row, int V, float m, float c, int ks,
+                            const uint32_t (&th)[kSplit], uint32_t hi, const Eligible& elig,
+                            RowShared& sh) {
   constexpr int E = Elt<T>::kPerUnit;
   const int nunits = (V + E - 1) / E;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned cnt[3] = {0, 0, 0};
-  unsigned long long mass[3] = {0, 0, 0};
+  const int lane = threadIdx.x & 31;
+  unsigned cnt[kSplit];
+  unsigned long long mass[kSplit];
+#pragma unroll
+  for (int t = 0; t < kSplit; ++t) { cnt[t] = 0; mass[t] = 0; }
   unsigned kmin = 0xffffffffu;
   for (int u = threadIdx.x; u < nunits; u += NT) {
     float f[E];
@@ -134,37 +160,37 @@ __device__ void tally3(const void* row, int V, float m, float c, int ks, const u
       if (i >= V) break;
       const uint32_t k = order_key(f[e]);
       if (!elig(k, i)) continue;
-      const uint32_t s = k >> ks;
-      kmin = min(kmin, s);
-      if (s >= th[0]) {
+      const uint32_t sk = k >> ks;
+      kmin = min(kmin, sk);
+      if (sk >= th[0] && sk <= hi) {
         const unsigned long long w = to_fixed(tempered_weight(f[e], m, c));
 #pragma unroll
-        for (int t = 0; t < 3; ++t)
-          if (s >= th[t]) { cnt[t] += 1; mass[t] += w; }
+        for (int t = 0; t < kSplit; ++t)
+          if (sk >= th[t]) { cnt[t] += 1; mass[t] += w; }
       }
     }
   }
 #pragma unroll
-  for (int t = 0; t < 3; ++t) {
+  for (int t = 0; t < kSplit; ++t) {
     cnt[t] = (unsigned)warp_sum_u64(cnt[t]);
     mass[t] = warp_sum_u64(mass[t]);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
-    for (int t = 0; t < 3; ++t) { sh.red_cnt[t] = 0; sh.red_mass[t] = 0; }
+    for (int t = 0; t < kSplit; ++t) { sh.red_cnt[t] = 0; sh.red_mass[t] = 0; }
     sh.red_min = 0xffffffffu;
   }
-  __syncthreads();
+  csync();
   if (lane == 0) {
-    for (int t = 0; t < 3; ++t) {
+    for (int t = 0; t < kSplit; ++t) {
       atomicAdd(&sh.red_cnt[t], cnt[t]);
       atomicAdd(&sh.red_mass[t], mass[t]);
     }
     atomicMin(&sh.red_min, kmin);
   }
-  __syncthreads();
+  csync();
 }
 
 // The j-th (1-based) eligible token with order key `key`, in index order.
@@ -192,7 +218,7 @@ __device__ int tie_cut(const void* row, int V, uint32_t key, unsigned j, const E
   unsigned long long bw, tw;
   block_exscan(mine, 0ull, base, bw, tot, tw, sh);
   if (threadIdx.x == 0) sh.tie_idx = -1;
-  __syncthreads();
+  csync();
   if (base < j && base + mine >= j) {
     unsigned want = j - base;
     for (int u = u_lo; u < u_hi && want; ++u) {
@@ -208,7 +234,7 @@ __device__ int tie_cut(const void* row, int V, uint32_t key, unsigned j, const E
       }
     }
   }
-  __syncthreads();
+  csync();
   return sh.tie_idx;
 }
 
@@ -216,58 +242,70 @@ template <typename T>
 __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by_mass,
                                unsigned need_count, uint64_t need_mass, Eligible elig,
                                RowShared& sh) {
-  const int ks = (sizeof(T) == 2) ? 16 : 0;  // bf16 keys carry 16 zero low bits
+  const int ks = (sizeof(T) == 2) ? 16 : 0;  // bf16 keys carry 16 constant low bits
   const uint32_t kmax = order_key(m) >> ks;
   auto reaches = [&](unsigned cnt, unsigned long long mass) {
     return by_mass ? (mass >= need_mass) : (cnt >= need_count);
   };
-  // first pass: the eligible totals and the smallest eligible key
-  uint32_t th0[3] = {0u, 0u, 0u};
-  tally3<T>(row, V, m, c, ks, th0, elig, sh);
+  // first pass: eligible totals and the smallest eligible key
+  uint32_t th[kSplit];
+  for (int t = 0; t < kSplit; ++t) th[t] = 0u;
+  tally_range<T>(row, V, m, c, ks, th, 0xffffffffu, elig, sh);
   uint64_t lo = sh.red_min, hi = kmax;
-  bool short_all = !reaches(sh.red_cnt[0], sh.red_mass[0]);
-  if (short_all) {
-    hi = lo;  // eligible mass short of the target (rounding): keep every eligible token
-  }
+  // tokens with a key above hi: their count and mass, carried from pass to pass
+  unsigned above_c = 0;
+  unsigned long long above_m = 0;
+  const unsigned total_c = sh.red_cnt[0];
+  const unsigned long long total_m = sh.red_mass[0];
+  const bool short_all = !reaches(total_c, total_m);
+  if (short_all) hi = lo;  // eligible mass short of the target (rounding): keep them all
   while (lo < hi) {
-    // three thresholds split (lo, hi] into four parts; keep the highest reaching part
-    uint64_t span = hi - lo;
-    uint32_t th[3];
-    for (int t = 0; t < 3; ++t) th[t] = (uint32_t)(lo + (span * (uint64_t)(t + 1) + 3) / 4);
-    tally3<T>(row, V, m, c, ks, th, elig, sh);
-    uint64_t nlo = lo, nhi = hi;
-    for (int t = 2; t >= 0; --t) {
-      if (reaches(sh.red_cnt[t], sh.red_mass[t])) { nlo = th[t]; break; }
-      nhi = (uint64_t)th[t] - 1;
+    const uint64_t span = hi - lo;
+    for (int t = 0; t < kSplit; ++t)
+      th[t] = (uint32_t)(lo + (span * (uint64_t)(t + 1) + kSplit) / (kSplit + 1));
+    tally_range<T>(row, V, m, c, ks, th, (uint32_t)hi, elig, sh);
+    int pick = -1;
+    for (int t = kSplit - 1; t >= 0; --t)
+      if (reaches(above_c + sh.red_cnt[t], above_m + sh.red_mass[t])) { pick = t; break; }
+    if (pick < 0) {
+      hi = (uint64_t)th[0] - 1;
+      above_c += sh.red_cnt[0];
+      above_m += sh.red_mass[0];
+    } else {
+      lo = th[pick];
+      if (pick < kSplit - 1) {
+        hi = (uint64_t)th[pick + 1] - 1;
+        above_c += sh.red_cnt[pick + 1];
+        above_m += sh.red_mass[pick + 1];
+      }
     }
-    lo = nlo;
-    hi = nhi;
   }
-  const uint32_t ks_key = (uint32_t)lo;
-  // tallies at and above the cut key
-  uint32_t th1[3] = {ks_key, ks_key + 1u, ks_key + 1u};
-  tally3<T>(row, V, m, c, ks, th1, elig, sh);
-  const unsigned cnt_ge = sh.red_cnt[0], cnt_gt = sh.red_cnt[1];
-  const unsigned long long mass_ge = sh.red_mass[0], mass_gt = sh.red_mass[1];
-  const unsigned cnt_eq = cnt_ge - cnt_gt;
-  const unsigned long long w_eq = cnt_eq ? (mass_ge - mass_gt) / cnt_eq : 0ull;
+  // the tokens carrying the cut key
+  const uint32_t kstar = (uint32_t)lo;
+  for (int t = 0; t < kSplit; ++t) th[t] = kstar;
+  tally_range<T>(row, V, m, c, ks, th, kstar, elig, sh);
+  const unsigned cnt_eq = sh.red_cnt[0];
+  const unsigned long long w_eq = cnt_eq ? sh.red_mass[0] / cnt_eq : 0ull;
   unsigned j;
   if (short_all) {
+    // every eligible token is kept; the cut is the last one, in the lowest key
+    above_c = total_c - cnt_eq;
+    above_m = total_m - sh.red_mass[0];
     j = cnt_eq;
   } else if (!by_mass) {
-    j = need_count - cnt_gt;
+    j = need_count - above_c;
   } else if (w_eq == 0) {
     j = cnt_eq;
   } else {
-    unsigned long long jj = (need_mass - mass_gt + w_eq - 1) / w_eq;
+    const unsigned long long jj = (need_mass - above_m + w_eq - 1) / w_eq;
     j = (unsigned)(jj < 1 ? 1 : (jj > cnt_eq ? cnt_eq : jj));
   }
-  const uint32_t key = ks ? key_from16(ks_key) : ks_key;
+  const uint32_t key = ks ? key_from16(kstar) : kstar;
   SelOut r;
   r.key = key;
   r.idx = tie_cut<T>(row, V, key, j, elig, sh);
-  r.kept = cnt_gt + j;
-  r.mass_kept = mass_gt + w_eq * j;
+  r.kept = above_c + j;
+  r.mass_kept = above_m + w_eq * j;
   return r;
 }
 
@@ -275,27 +313,259 @@ __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by
 // The row pass kernel.  MODE 0: greedy (max + argmax only).  MODE 1: sampling
 // without truncation.  MODE 2: sampling with top-k and/or top-p.
 // ---------------------------------------------------------------------------
+// Candidate entries.  bf16: one 32-bit word, the vocabulary index above the key's
+// offset from the row's floor key (fixed after the first iteration; every later
+// window threshold is higher, so offsets are never negative).  fp32: (index, bits).
+template <typename T> struct Cand;
+template <> struct Cand<uint16_t> {
+  static constexpr int kCap = kCandCapBf16;
+  using entry_t = uint32_t;
+  __device__ __forceinline__ static uint4 neg_inf() {
+    return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  }
+  __device__ __forceinline__ static uint4 partial(const void* row, int V, int u) {
+    uint32_t w[4];
+    const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i0 = u * 8 + 2 * q, i1 = i0 + 1;
+      const uint32_t lo = i0 < V ? (uint32_t)__ldg(r + i0) : 0xff80u;
+      const uint32_t hi = i1 < V ? (uint32_t)__ldg(r + i1) : 0xff80u;
+      w[q] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <> struct Cand<float> {
+  static constexpr int kCap = kCandCapF32;
+  using entry_t = uint2;
+  __device__ __forceinline__ static uint4 neg_inf() {
+    return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+  }
+  __device__ __forceinline__ static uint4 partial(const void* row, int V, int u) {
+    uint32_t w[4];
+    const float* r = reinterpret_cast<const float*>(row);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = u * 4 + q;
+      w[q] = i < V ? __float_as_uint(__ldg(r + i)) : 0xff800000u;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Dynamic shared memory: the ring, its full / empty barriers, the candidate
+// regions, and the selection scratch (histogram, bin weights, ties; or the sort
+// keys of an fp32 window).
+constexpr size_t kRingBytes = (size_t)kRingStages * kStageBytes;
+constexpr size_t kBarBytes = (size_t)kRingStages * 16;
+constexpr size_t kScratchBytes = (size_t)kHistBins * 12 + (size_t)kTieCap * 4 > (size_t)kSortCap * 8
+                                     ? (size_t)kHistBins * 12 + (size_t)kTieCap * 4
+                                     : (size_t)kSortCap * 8;
+template <typename T>
+__host__ __device__ constexpr size_t cand_bytes() {
+  return (size_t)Cand<T>::kCap * sizeof(typename Cand<T>::entry_t);
+}
+template <typename T>
+__host__ __device__ constexpr size_t row_dyn_smem() {
+  return kRingBytes + kBarBytes + cand_bytes<T>() + kScratchBytes;
+}
+
+// 16-bit order key of the bf16 logit with raw bits b.
+__device__ __forceinline__ uint32_t key16_bits(uint32_t b) {
+  return order_key(__uint_as_float(b << 16)) >> 16;
+}
+
+// Maximum of a thread's U units: packed bf16x2 maxima for bf16 logits (NaN-propagating
+// when asked), fmaxf for fp32.
+template <typename T, bool PROPAGATE_NAN>
+__device__ __forceinline__ float packed_max(const uint4 (&raw)[kRingUnits]) {
+  if constexpr (sizeof(T) == 2) {
+    __nv_bfloat162 m2 = bf2(raw[0].x);
+#pragma unroll
+    for (int k = 0; k < kRingUnits; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int q = (k == 0 ? 1 : 0); q < 4; ++q)
+        m2 = PROPAGATE_NAN ? __hmax2_nan(m2, bf2(w[q])) : __hmax2(m2, bf2(w[q]));
+    }
+    const float lo = __low2float(m2), hi = __high2float(m2);
+    return PROPAGATE_NAN ? ((lo != lo || hi != hi) ? CUDART_NAN_F : fmaxf(lo, hi)) : fmaxf(lo, hi);
+  } else {
+    float m = -CUDART_INF_F;
+    int nan = 0;
+#pragma unroll
+    for (int k = 0; k < kRingUnits; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float v = __uint_as_float(w[q]);
+        m = fmaxf(m, v);
+        if (PROPAGATE_NAN) nan |= (v != v);
+      }
+    }
+    return (PROPAGATE_NAN && nan) ? CUDART_NAN_F : m;
+  }
+}
+
+// Window membership bits of a thread's units (a superset is fine: the final window
+// is re-filtered exactly).  bf16: compares against the threshold rounded down to
+// bf16, two logits per instruction; bit p = low half of word p, bit p + 16 = high
+// half.  fp32: bit p = word p.
+template <typename T>
+__device__ __forceinline__ unsigned window_mask(const uint4 (&raw)[kRingUnits],
+                                                const float (&f)[kRingUnits][Elt<T>::kPerUnit],
+                                                __nv_bfloat162 t2, float thr) {
+  unsigned mask = 0;
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int k = 0; k < kRingUnits; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int p = k * 4 + q;
+        mask |= __hge2_mask(bf2(w[q]), t2) & ((1u << p) | (1u << (p + 16)));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kRingUnits; ++k)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mask |= (f[k][e] >= thr) ? (1u << (k * 4 + e)) : 0u;
+  }
+  return mask;
+}
+
+// Unit k, element e and the shared-memory byte offset (within the stage) of the
+// logit named by a window bit.
+template <typename T>
+__device__ __forceinline__ uint32_t window_slot(int bit, int& k, int& e) {
+  static_assert(kRingUnits * 4 <= 16, "window bits are laid out for up to 16 words per thread");
+  if constexpr (sizeof(T) == 2) {
+    const int p = bit & 15, half = bit >> 4;
+    k = p >> 2;
+    const int q = p & 3;
+    e = 2 * q + half;
+    return (uint32_t)((k * NT + (int)threadIdx.x) * 16 + q * 4 + half * 2);
+  } else {
+    k = bit >> 2;
+    e = bit & 3;
+    return (uint32_t)((k * NT + (int)threadIdx.x) * 16 + e * 4);
+  }
+}
+
 template <typename T, int MODE>
-__global__ void __launch_bounds__(NT, kRowBlocksPerSm) row_pass_kernel(RowJob job) {
+__global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kernel(RowJob job) {
   constexpr int E = Elt<T>::kPerUnit;
+  constexpr int U = kRingUnits;
+  constexpr int S = kRingStages;
+  constexpr int CAP = Cand<T>::kCap;
+  constexpr int CAPW = CAP / NW;  // candidate region of one warp
+  using entry_t = typename Cand<T>::entry_t;
   __shared__ RowShared sh;
-  extern __shared__ __align__(16) unsigned char dyn[];
-  uint2* cand = reinterpret_cast<uint2*>(dyn);  // (index, logit bits)
-  unsigned long long* pre = reinterpret_cast<unsigned long long*>(dyn);  // reuses cand
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(dyn + (size_t)kCandCap * 8);
-  unsigned* hist = reinterpret_cast<unsigned*>(dyn + (size_t)kCandCap * 8);  // aliases keys
-  unsigned* ties = hist + kHistBins;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  uint4* ring = reinterpret_cast<uint4*>(dyn);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(dyn + kRingBytes);
+  uint64_t* empty_bar = full_bar + S;
+  entry_t* cand = reinterpret_cast<entry_t*>(dyn + kRingBytes + kBarBytes);
+  unsigned char* scratch = dyn + kRingBytes + kBarBytes + cand_bytes<T>();
+  unsigned* hist = reinterpret_cast<unsigned*>(scratch);
+  unsigned long long* wbin = reinterpret_cast<unsigned long long*>(scratch + (size_t)kHistBins * 4);
+  unsigned* ties = reinterpret_cast<unsigned*>(scratch + (size_t)kHistBins * 12);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(scratch);
+  unsigned long long* pre = reinterpret_cast<unsigned long long*>(cand);  // after compaction
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int V = job.V;
   const int nunits = (V + E - 1) / E;
   const int full_units = V / E;
+  const int per_iter = NT * U;
+  const int niter = (nunits + per_iter - 1) / per_iter;
   const float c = job.c;
   const int BN = job.B * job.N;
   const int total = (job.mode == kRowsList) ? job.R : (job.with_q ? 2 * BN : BN);
   const bool topk_on = job.top_k > 0 && job.top_k < V;
   const bool topp_on = job.top_p < 1.0f;
+  entry_t* region = cand + (warp < NW ? warp : 0) * CAPW;
+  const uint64_t limit = job.wait_limit_ns;
+  const uint32_t row_bytes = (uint32_t)V * Elt<T>::kBytes;
+  const uint32_t row_bytes16 = row_bytes & ~15u;   // the part the bulk copies move
+  const int nchunks = (int)((row_bytes + kStageBytes - 1) / kStageBytes);
 
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full_bar[i], 1);       // the producer's arrive + the copy's bytes
+      mbar_init(&empty_bar[i], NW);     // one arrive per consumer warp
+    }
+    sh.tmo = 0;
+    sh.run_key = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ---------------- producer warp ----------------
+    uint32_t g = 0;  // chunks issued so far (the same count the consumers walk)
+    bool stop = false;
+    for (int v = blockIdx.x; v < total && !stop; v += gridDim.x) {
+      const char* row;
+      if (job.mode == kRowsList) {
+        row = static_cast<const char*>(row_ptr(job.base_p, (int64_t)v * job.row_pitch, Elt<T>::kBytes));
+      } else {
+        const bool is_q = v >= BN;
+        const int r = is_q ? v - BN : v;
+        const int b = r / job.N, n = r - b * job.N;
+        if (is_q) {
+          int has_child = 0;
+          for (int ch = n + 1 + lane; ch < job.N; ch += 32)
+            has_child |= (job.parents[(int64_t)b * job.N + ch] == n);
+          if (!__any_sync(kFull, has_child)) continue;
+        }
+        const int64_t off = (int64_t)b * job.batch_stride + (int64_t)n * job.row_pitch;
+        row = static_cast<const char*>(row_ptr(is_q ? job.base_q : job.base_p, off, Elt<T>::kBytes));
+      }
+      for (int ck = 0; ck < nchunks; ++ck, ++g) {
+        // lane 0 waits and issues; the warp follows its decision
+        int go = 0;
+        if (lane == 0) {
+          const int st = (int)(g % S);
+          const uint32_t use = g / S;
+          if (!*((volatile int*)&sh.tmo)) {
+            if (mbar_wait(&empty_bar[st], (use & 1u) ^ 1u, limit)) {
+              const uint32_t off = (uint32_t)ck * kStageBytes;
+              const uint32_t bytes =
+                  off < row_bytes16 ? min((uint32_t)kStageBytes, row_bytes16 - off) : 0u;
+              // the stall self-test announces 16 bytes more than the copy delivers, so
+              // this phase never completes and the consumers' bounded wait runs out;
+              // nothing more is issued after it
+              const bool stall = (job.flags & SPEC_FLAG_TEST_STALL) && g == 1;
+              mbar_arrive_expect_tx(&full_bar[st], bytes + (stall ? 16u : 0u));
+              if (bytes) bulk_copy_g2s(ring + (size_t)st * U * NT, row + off, bytes, &full_bar[st]);
+              go = stall ? 2 : 1;
+            } else {
+              atomicExch(&sh.tmo, 1);
+            }
+          }
+        }
+        go = __shfl_sync(kFull, go, 0);
+        if (go != 1) {
+          if (go == 2) ++g;  // the withheld chunk was issued
+          stop = true;
+          break;
+        }
+      }
+    }
+    // no copy may still be landing when the block exits: wait (bounded) for the
+    // last stages issued
+    if (lane == 0) {
+      const uint32_t first = g > (uint32_t)S ? g - S : 0u;
+      for (uint32_t h = first; h < g; ++h) mbar_wait(&full_bar[h % S], (h / S) & 1u, limit);
+    }
+    return;
+  }
+
+  // ---------------- consumer threads ----------------
+  uint32_t g = 0;
   for (int v = blockIdx.x; v < total; v += gridDim.x) {
     const void* row;
     spec_row_stats* out;
@@ -305,181 +575,224 @@ __global__ void __launch_bounds__(NT, kRowBlocksPerSm) row_pass_kernel(RowJob jo
     } else {
       const bool is_q = v >= BN;
       const int r = is_q ? v - BN : v;
-      if (is_q && !job.need_q[r]) continue;
       const int b = r / job.N, n = r - b * job.N;
+      if (is_q) {
+        // the draft row of node n is read only if some node has n as its parent
+        // (every warp decides for itself, identically)
+        int has_child = 0;
+        for (int ch = n + 1 + lane; ch < job.N; ch += 32)
+          has_child |= (job.parents[(int64_t)b * job.N + ch] == n);
+        if (!__any_sync(kFull, has_child)) continue;
+      }
       const int64_t off = (int64_t)b * job.batch_stride + (int64_t)n * job.row_pitch;
       row = row_ptr(is_q ? job.base_q : job.base_p, off, Elt<T>::kBytes);
       out = (is_q ? job.stats_q : job.stats_p) + r;
     }
-    if (threadIdx.x == 0) {
-      sh.n_cand = 0;
-      sh.run_key = 0u;
-    }
-    __syncthreads();
+    // the block-wide running maximum starts afresh for every row (all reads of the
+    // previous row's value happened before that row's last barrier)
+    if (threadIdx.x == 0) sh.run_key = 0u;
+    csync();
 
     // ---------------- streaming pass ----------------
     float Mw = -CUDART_INF_F;
-    Kahan S;
-    float best = -CUDART_INF_F;
-    int best_idx = INT_MAX;
+    Kahan Sk;
+    float best = -CUDART_INF_F;  // warp-uniform: the warp's maximum so far
+    int best_idx = INT_MAX;      // and its lowest vocabulary index
     int bad = 0;
-    const uint4* row4 = reinterpret_cast<const uint4*>(row);
-    for (int u0 = 0; u0 < nunits; u0 += NT * kUnroll) {
-      float f[kUnroll][E];
+    unsigned wcount = 0;     // warp-uniform: entries this warp appended
+    int overflow = 0;
+    uint32_t floor16 = 0;    // bf16: key of the first window threshold
+    const int full_iters = full_units / per_iter;  // iterations with no partial unit
+    for (int it = 0; it < niter; ++it, ++g) {
+      const int sidx = (int)(g % S);
+      if (!*((volatile int*)&sh.tmo) && !mbar_wait(&full_bar[sidx], (g / S) & 1u, limit))
+        atomicExch(&sh.tmo, 1);
+      uint4* st = ring + (size_t)sidx * U * NT;
+      uint4 raw[U];
+      if (it < full_iters) {
 #pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const int u = u0 + k * NT + threadIdx.x;
-        if (u < full_units) {
-          uint4 raw = __ldg(row4 + u);
-          Elt<T>::unpack(raw, f[k]);
-        } else if (u < nunits) {
-          load_unit<T>(row, V, u, f[k]);
-        } else {
+        for (int k = 0; k < U; ++k) raw[k] = st[k * NT + threadIdx.x];
+      } else {
+        // the last chunk: units past the bulk copy are loaded here and parked in this
+        // thread's own slots of the stage, so the window can read them back
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[k][e] = -CUDART_INF_F;
+        for (int k = 0; k < U; ++k) {
+          const int u = it * per_iter + k * NT + threadIdx.x;
+          if (u < full_units) {
+            raw[k] = st[k * NT + threadIdx.x];
+          } else {
+            raw[k] = u < nunits ? Cand<T>::partial(row, V, u) : Cand<T>::neg_inf();
+            st[k * NT + threadIdx.x] = raw[k];
+          }
         }
       }
-      float tmax = -CUDART_INF_F;
-#pragma unroll
-      for (int k = 0; k < kUnroll; ++k)
-#pragma unroll
-        for (int e = 0; e < E; ++e) tmax = fmaxf(tmax, f[k][e]);
-      if (tmax > best) {
+      const float tmax = packed_max<T, MODE == 0>(raw);
+      const float wm = warp_max(tmax);
+      if (wm > best) {
+        // the warp maximum improved (a warp-uniform branch): every lane holding it
+        // finds its first position (increasing unit, then element, is increasing
+        // vocabulary index within a lane) and the warp keeps the lowest index
         int idx = INT_MAX;
+        if (tmax == wm) {
 #pragma unroll
-        for (int k = kUnroll - 1; k >= 0; --k)
+          for (int k = U - 1; k >= 0; --k) {
+            float fk[E];
+            Elt<T>::unpack(raw[k], fk);
 #pragma unroll
-          for (int e = E - 1; e >= 0; --e)
-            if (f[k][e] == tmax) idx = (u0 + k * NT + threadIdx.x) * E + e;
-        best = tmax;
-        best_idx = idx;
+            for (int e = E - 1; e >= 0; --e)
+              if (fk[e] == wm) idx = (it * per_iter + k * NT + threadIdx.x) * E + e;
+          }
+        }
+        best = wm;
+        best_idx = warp_min_i(idx);
       }
       if (MODE == 0) {
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k)
-#pragma unroll
-          for (int e = 0; e < E; ++e) bad |= (f[k][e] != f[k][e]);
-        continue;
-      }
-      const float wm = warp_max(tmax);
-      if (MODE == 2) {
-        // publish the warp maximum; the first iteration waits for every warp so that
-        // the window starts from a block-wide maximum
-        if (lane == 0 && wm > -CUDART_INF_F) atomicMax(&sh.run_key, order_key(wm));
-        if (u0 == 0) __syncthreads();
-      }
-      if (wm > Mw) {
-        if (Mw != -CUDART_INF_F) {
-          const float scale = ex2_approx((Mw - wm) * c);
-          S.s *= scale;
-          S.c *= scale;
-        }
-        Mw = wm;
-      }
-      if (Mw == -CUDART_INF_F) {  // nothing finite yet: only NaN can hide here
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k)
-#pragma unroll
-          for (int e = 0; e < E; ++e) bad |= (f[k][e] != f[k][e]);
-        continue;
-      }
-      const float negMc = -Mw * c;
-      float part = 0.f;
-#pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        float pk = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) pk += ex2_approx(fmaf(f[k][e], c, negMc));
-        part += pk;
-      }
-      S.add(part);
-      if (MODE == 2) {
-        const unsigned rk = *((volatile unsigned*)&sh.run_key);
-        const float bmax = rk ? fmaxf(Mw, key_value(rk)) : Mw;
-        const float thr = bmax - job.delta_z;
-        int mine = 0;
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k)
-#pragma unroll
-          for (int e = 0; e < E; ++e) mine += (f[k][e] >= thr);
-        if (__any_sync(kFull, mine > 0)) {
-          int incl = mine;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += t;
+        bad |= (tmax != tmax);  // the NaN-propagating maximum flags a NaN
+      } else {
+        if (MODE == 2) {
+          // publish the warp maximum; the first iteration waits for every warp so that
+          // the window starts from a block-wide maximum
+          if (lane == 0 && wm > -CUDART_INF_F) atomicMax(&sh.run_key, order_key(wm));
+          if (it == 0) {
+            csync();
+            const unsigned rk0 = sh.run_key;
+            if (sizeof(T) == 2 && rk0)
+              floor16 = order_key(__bfloat162float(
+                            __float2bfloat16_rd(key_value(rk0) - job.delta_z))) >> 16;
           }
-          unsigned base = 0;
-          if (lane == 31) base = atomicAdd(&sh.n_cand, (unsigned)incl);
-          base = __shfl_sync(kFull, base, 31);
-          unsigned pos = base + incl - mine;
+        }
+        if (wm > Mw) {
+          if (Mw != -CUDART_INF_F) {
+            const float scale = ex2_approx((Mw - wm) * c);
+            Sk.s *= scale;
+            Sk.c *= scale;
+          }
+          Mw = wm;
+        }
+        float f[U][E];
 #pragma unroll
-          for (int k = 0; k < kUnroll; ++k)
+        for (int k = 0; k < U; ++k) Elt<T>::unpack(raw[k], f[k]);
+        if (Mw == -CUDART_INF_F) {  // nothing finite yet: only NaN can hide here
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-              if (f[k][e] >= thr) {
-                if (pos < (unsigned)kCandCap)
-                  cand[pos] = make_uint2((unsigned)((u0 + k * NT + threadIdx.x) * E + e),
-                                         __float_as_uint(f[k][e]));
+          for (int k = 0; k < U; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) bad |= (f[k][e] != f[k][e]);
+        } else {
+          // 2^((z - Mw) c) for pairs of logits: packed fp32 FMAs and adds
+          const float negMc = -Mw * c;
+          const float2 c2 = make_float2(c, c), n2 = make_float2(negMc, negMc);
+          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int k = 0; k < U; ++k)
+#pragma unroll
+            for (int e = 0; e < E; e += 2) {
+              const float2 a = __ffma2_rn(make_float2(f[k][e], f[k][e + 1]), c2, n2);
+              acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+            }
+          const float2 tot = __fadd2_rn(acc[0], acc[1]);
+          Sk.add(tot.x + tot.y);
+          if (MODE == 2) {
+            const unsigned rk = *((volatile unsigned*)&sh.run_key);
+            const float bmax = rk ? fmaxf(Mw, key_value(rk)) : Mw;
+            const float thr = bmax - job.delta_z;
+            const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(thr));
+            unsigned mask = window_mask<T>(raw, f, t2, thr);
+            if (__any_sync(kFull, mask != 0)) {
+              // append to this warp's region; no atomics: offsets from a warp scan
+              const unsigned mine = __popc(mask);
+              unsigned incl = mine;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const unsigned t = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += t;
+              }
+              unsigned pos = wcount + incl - mine;
+              wcount += __shfl_sync(kFull, incl, 31);
+              const unsigned char* stb = reinterpret_cast<const unsigned char*>(st);
+              while (mask) {
+                const int bit = __ffs(mask) - 1;
+                mask &= mask - 1;
+                int k, e;
+                const uint32_t off = window_slot<T>(bit, k, e);
+                const uint32_t idx = (uint32_t)((it * per_iter + k * NT + threadIdx.x) * E + e);
+                if constexpr (sizeof(T) == 2) {
+                  const uint32_t zb = *reinterpret_cast<const unsigned short*>(stb + off);
+                  const uint32_t rel = key16_bits(zb) - floor16;
+                  if (pos < (unsigned)CAPW && rel < (uint32_t)kHistBins)
+                    region[pos] = (idx << kKeySpanBits) | rel;
+                  else
+                    overflow = 1;
+                } else {
+                  const uint32_t zb = *reinterpret_cast<const uint32_t*>(stb + off);
+                  if (pos < (unsigned)CAPW) region[pos] = make_uint2(idx, zb);
+                  else overflow = 1;
+                }
                 ++pos;
               }
+            }
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[sidx]);  // this warp is done with the stage
     }
-
     // ---------------- block combine ----------------
     {
-      const double ws = warp_sum_d(S.value());
-      const float wb = warp_max(best);
-      const int wi = warp_min_i(best == wb ? best_idx : INT_MAX);
+      const FF ws = warp_sum_ff(Sk.ff());
+      const float wb = best;
       const int wbad = __any_sync(kFull, bad);
+      const int wof = __any_sync(kFull, overflow);
       if (lane == 0) {
         sh.warp_m[warp] = Mw;
-        sh.warp_s[warp] = ws;
+        sh.warp_s[warp] = ws.value();
         sh.warp_best[warp] = wb;
-        sh.warp_best_idx[warp] = wi;
         sh.warp_bad[warp] = wbad;
+        sh.wcnt[warp] = wcount;
+        sh.woverflow[warp] = wof || wcount > (unsigned)CAPW;
       }
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) {
       float m = -CUDART_INF_F;
-      int am = INT_MAX, anybad = 0;
+      int anybad = 0;
       for (int w = 0; w < NW; ++w) {
-        const float b = sh.warp_best[w];
-        if (b > m) { m = b; am = sh.warp_best_idx[w]; }
-        else if (b == m) am = min(am, sh.warp_best_idx[w]);
+        m = fmaxf(m, sh.warp_best[w]);
         anybad |= sh.warp_bad[w];
       }
       double s = 0.0;
       if (MODE != 0) {
         for (int w = 0; w < NW; ++w)
-          if (sh.warp_m[w] != -CUDART_INF_F)
-            s += sh.warp_s[w] * exp2(((double)sh.warp_m[w] - (double)m) * (double)c);
+          if (sh.warp_m[w] != -CUDART_INF_F) s += sh.warp_s[w] * (double)exp2f((sh.warp_m[w] - m) * c);
       }
       const bool finite = !anybad && m != CUDART_INF_F && m != -CUDART_INF_F && !(m != m) &&
                           (MODE == 0 || (s == s && s != CUDART_INF));
       sh.m = m;
       sh.s_total = s;
-      sh.argmax = (am == INT_MAX) ? 0 : am;
-      sh.bad = !finite;
+      sh.argmax = INT_MAX;
+      // a timed-out wait leaves the row's data unknown
+      sh.bad = *((volatile int*)&sh.tmo) ? SPEC_ROW_TIMEOUT : (finite ? 0 : SPEC_ROW_NONFINITE);
       if (job.counters) {
         atomicAdd(&job.counters[0], 1ull);
         atomicAdd(&job.counters[1], (unsigned long long)V * Elt<T>::kBytes);
       }
     }
-    __syncthreads();
+    csync();
+    // argmax: the lowest index among the warps holding the maximum
+    if (lane == 0 && best == sh.m && best_idx != INT_MAX) atomicMin(&sh.argmax, best_idx);
+    csync();
+    if (threadIdx.x == 0 && sh.argmax == INT_MAX) sh.argmax = 0;
+    csync();
     const float m = sh.m;
     const int argmax = sh.argmax;
 
     if (sh.bad) {
       if (threadIdx.x == 0) {
         spec_row_stats st;
-        st.m = m; st.status = SPEC_ROW_NONFINITE; st.s_f = 0.0; st.cut_key = 0;
+        st.m = m; st.status = sh.bad; st.s_f = 0.0; st.cut_key = 0;
         st.cut_idx = -1; st.argmax = argmax; st.kept = 0;
         *out = st;
       }
-      __syncthreads();
+      csync();
       continue;
     }
     if (MODE == 0 || MODE == 1) {
@@ -495,7 +808,7 @@ __global__ void __launch_bounds__(NT, kRowBlocksPerSm) row_pass_kernel(RowJob jo
         }
         *out = st;
       }
-      __syncthreads();
+      csync();
       continue;
     }
 
@@ -508,225 +821,266 @@ __global__ void __launch_bounds__(NT, kRowBlocksPerSm) row_pass_kernel(RowJob jo
     int cut_idx = 0;
     unsigned kept = 0;
     uint64_t sf_fixed = 0;
-    const unsigned n_buf = sh.n_cand;
     const float thr = m - job.delta_z;
-    const uint32_t K16m = order_key(m) >> 16;
-    const uint32_t K16thr = order_key(thr) >> 16;
-    const bool use_hist = (sizeof(T) == 2) && (K16m - K16thr < (uint32_t)kHistBins);
-    if (!(job.flags & SPEC_FLAG_EXACT_SELECT) && n_buf <= (unsigned)kCandCap && use_hist) {
-      // ---- bf16 window: one bin per key below the maximum ----
-      const int nb = (int)(K16m - K16thr) + 1;
-      for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
-      if (threadIdx.x == 0) { sh.first = INT_MAX; sh.ok = 1; sh.tie_n = 0; sh.tie_idx = -1; }
-      __syncthreads();
-      for (unsigned i = threadIdx.x; i < n_buf; i += NT) {
-        const float z = __uint_as_float(cand[i].y);
-        if (z >= thr) atomicAdd(&hist[K16m - (order_key(z) >> 16)], 1u);
-      }
-      __syncthreads();
-      // per-thread chunk of bins; bin b holds the key b steps below the maximum, and
-      // its weight is the weight of that key
-      const int b_lo = threadIdx.x * kBinsPerThread;
-      auto bin_w = [&](int bin) -> unsigned long long {
-        return to_fixed(tempered_weight(key_value(key_from16(K16m - (uint32_t)bin)), m, c));
-      };
-      unsigned lc = 0;
-      unsigned long long lw = 0;
-      for (int t = 0; t < kBinsPerThread; ++t) {
-        const int bin = b_lo + t;
-        if (bin < nb && hist[bin]) { lc += hist[bin]; lw += (unsigned long long)hist[bin] * bin_w(bin); }
-      }
-      unsigned base_c, tot_c;
-      unsigned long long base_w, tot_w;
-      block_exscan(lc, lw, base_c, base_w, tot_c, tot_w, sh);
-      // top-k: the bin holding the K-th token
-      int b_k = nb;  // "no top-k": past the last bin
-      unsigned jk = 0;
-      unsigned long long s_k_fixed = 0;
-      if (topk_on) {
-        if (tot_c < K) {
-          if (threadIdx.x == 0) sh.ok = 0;
-        } else {
-          unsigned rc = base_c;
-          for (int t = 0; t < kBinsPerThread; ++t) {
-            const int bin = b_lo + t;
-            if (bin >= nb) break;
-            if (rc + hist[bin] >= K) { atomicMin(&sh.first, bin); break; }
-            rc += hist[bin];
+    int any_overflow = 0;
+    for (int w = 0; w < NW; ++w) any_overflow |= sh.woverflow[w];
+    const bool window_ok = !(job.flags & SPEC_FLAG_EXACT_SELECT) && !any_overflow;
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t K16m = order_key(m) >> 16;
+      const uint32_t K16thr = order_key(thr) >> 16;  // lowest key the window can hold
+      // a stored maximum bounds the window by kHistBins keys; check it regardless and
+      // leave any wider window to the exact selection
+      const bool fits = K16m - K16thr < (uint32_t)kHistBins;
+      if (window_ok && fits) {
+        // ---- bf16 window: one bin per key below the maximum ----
+        const int nb = (int)(K16m - K16thr) + 1;
+        for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
+        csync();
+        {
+          const int n_own = min((int)sh.wcnt[warp], CAPW);  // each warp reads its own region
+          for (int i = lane; i < n_own; i += 32) {
+            const uint32_t k16 = floor16 + (region[i] & (kHistBins - 1));
+            const uint32_t bin = K16m - k16;
+            if (bin < (uint32_t)nb && key_value(key_from16(k16)) >= thr) atomicAdd(&hist[bin], 1u);
           }
         }
-        __syncthreads();
-        if (sh.ok) {
-          b_k = sh.first;
-          // counts / masses before b_k, owned by the thread whose chunk holds b_k
-          if (b_k >= b_lo && b_k < b_lo + kBinsPerThread) {
-            unsigned rc = base_c;
-            unsigned long long rw = base_w;
-            for (int bin = b_lo; bin < b_k; ++bin) { rc += hist[bin]; rw += (unsigned long long)hist[bin] * bin_w(bin); }
-            const unsigned j = K - rc;
-            sh.sel_j = j;
-            sh.tau = rw + (unsigned long long)j * bin_w(b_k);  // mass of the top-k set
-            sh.n_keep = rc;
-            sh.warp_mass[0] = rw;
+        csync();
+        if (warp == 0) {
+          // one warp scans the bins in key order: lane l owns bins [l*C, (l+1)*C)
+          const int C = (nb + 31) / 32;
+          const int b_lo = lane * C, b_hi = min(nb, b_lo + C);
+          unsigned lc = 0;
+          unsigned long long lw = 0;
+          for (int bin = b_lo; bin < b_hi; ++bin) {
+            const unsigned long long wgt =
+                to_fixed(tempered_weight(key_value(key_from16(K16m - (uint32_t)bin)), m, c));
+            wbin[bin] = wgt;
+            lc += hist[bin];
+            lw += (unsigned long long)hist[bin] * wgt;
           }
-          __syncthreads();
-          jk = sh.sel_j;
-          s_k_fixed = sh.tau;
-          if (!topp_on) {
-            cut_key = key_from16(K16m - (uint32_t)b_k);
-            kept = sh.n_keep + jk;
-            sf_fixed = s_k_fixed;
+          unsigned ic = lc;
+          unsigned long long iw = lw;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned tc = __shfl_up_sync(kFull, ic, o);
+            const unsigned long long tw = __shfl_up_sync(kFull, iw, o);
+            if (lane >= o) { ic += tc; iw += tw; }
           }
-        }
-      }
-      __syncthreads();
-      int b_cut = b_k;
-      unsigned j_cut = jk;
-      if (sh.ok && topp_on) {
-        const unsigned long long tau = (unsigned long long)ceil(
-            (double)job.top_p * (topk_on ? (double)s_k_fixed : s_total * tau_scale));
-        if (threadIdx.x == 0) sh.first = INT_MAX;
-        __syncthreads();
-        // masses up to b_k (bin b_k only counts its first jk tokens)
-        unsigned long long rw = base_w;
-        for (int t = 0; t < kBinsPerThread; ++t) {
-          const int bin = b_lo + t;
-          if (bin >= nb || bin > b_k) break;
-          const unsigned cnt = (bin == b_k) ? jk : hist[bin];
-          const unsigned long long w = (unsigned long long)cnt * bin_w(bin);
-          if (cnt && rw + w >= tau) { atomicMin(&sh.first, bin); break; }
-          rw += w;
-        }
-        __syncthreads();
-        if (sh.first == INT_MAX) {
-          if (threadIdx.x == 0) sh.ok = 0;  // the window holds too little mass
-        } else {
-          const int b_p = sh.first;
-          if (b_p >= b_lo && b_p < b_lo + kBinsPerThread) {
-            unsigned rc = base_c;
-            unsigned long long rw2 = base_w;
-            for (int bin = b_lo; bin < b_p; ++bin) { rc += hist[bin]; rw2 += (unsigned long long)hist[bin] * bin_w(bin); }
-            const unsigned avail = (b_p == b_k) ? jk : hist[b_p];
-            const unsigned long long w1 = bin_w(b_p);
-            unsigned j = avail;
-            if (w1 > 0) {
-              const unsigned long long jj = (tau - rw2 + w1 - 1) / w1;
-              j = (unsigned)(jj < 1 ? 1 : (jj > avail ? avail : jj));
-            }
-            sh.sel_j = j;
-            sh.n_keep = rc;
-            sh.warp_mass[0] = rw2 + (unsigned long long)j * w1;
-          }
-          __syncthreads();
-          b_cut = b_p;
-          j_cut = sh.sel_j;
-          cut_key = key_from16(K16m - (uint32_t)b_p);
-          kept = sh.n_keep + j_cut;
-          sf_fixed = sh.warp_mass[0];
-        }
-        __syncthreads();
-      }
-      if (sh.ok) {
-        // the j_cut-th token of the cut key in index order: rank its members
-        if (hist[b_cut] > (unsigned)kTieCap) {
-          if (threadIdx.x == 0) sh.ok = 0;
-        } else {
-          for (unsigned i = threadIdx.x; i < n_buf; i += NT) {
-            const uint2 e = cand[i];
-            if (order_key(__uint_as_float(e.y)) == cut_key) ties[atomicAdd(&sh.tie_n, 1u)] = e.x;
-          }
-          __syncthreads();
-          const unsigned nt = sh.tie_n;
-          for (unsigned i = threadIdx.x; i < nt; i += NT) {
-            const unsigned me = ties[i];
-            unsigned rank = 0;
-            for (unsigned t = 0; t < nt; ++t) rank += (ties[t] < me);
-            if (rank + 1 == j_cut) sh.tie_idx = (int)me;
-          }
-        }
-        __syncthreads();
-        cut_idx = sh.tie_idx;
-      }
-      __syncthreads();
-      done = sh.ok;
-      __syncthreads();
-    } else if (!(job.flags & SPEC_FLAG_EXACT_SELECT) && n_buf <= (unsigned)kCandCap) {
-      // ---- sorted window (fp32 logits, or a bf16 window spanning many keys) ----
-      if (threadIdx.x == 0) sh.n_keep = 0;
-      __syncthreads();
-      for (unsigned i = threadIdx.x; i < n_buf; i += NT) {
-        const uint2 e = cand[i];
-        const float z = __uint_as_float(e.y);
-        if (z >= thr) {
-          const unsigned pos = atomicAdd(&sh.n_keep, 1u);
-          if (pos < (unsigned)kSortCap)
-            keys[pos] = ((unsigned long long)order_key(z) << 32) | (unsigned long long)(~e.x);
-        }
-      }
-      __syncthreads();
-      const unsigned n_c = sh.n_keep;
-      if (n_c >= 1 && n_c <= (unsigned)kSortCap && (!topk_on || n_c >= K)) {
-        unsigned n_pad = 2;
-        while (n_pad < n_c) n_pad <<= 1;
-        for (unsigned i = n_c + threadIdx.x; i < n_pad; i += NT) keys[i] = 0ull;
-        __syncthreads();
-        for (unsigned k = 2; k <= n_pad; k <<= 1) {  // bitonic sort, descending
-          for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
-            for (unsigned i = threadIdx.x; i < n_pad; i += NT) {
-              const unsigned ixj = i ^ jj;
-              if (ixj > i) {
-                const unsigned long long a = keys[i], b = keys[ixj];
-                const bool swap = ((i & k) == 0) ? (a < b) : (a > b);
-                if (swap) { keys[i] = b; keys[ixj] = a; }
+          const unsigned base_c = ic - lc, tot_c = __shfl_sync(kFull, ic, 31);
+          const unsigned long long base_w = iw - lw;
+          int ok = 1;
+          int b_k = nb;  // no top-k: past the last bin
+          unsigned jk = 0;
+          unsigned long long s_k = 0;
+          if (topk_on) {
+            if (tot_c < K) {
+              ok = 0;
+            } else {
+              int hitbin = INT_MAX;
+              unsigned rc = base_c;
+              for (int bin = b_lo; bin < b_hi; ++bin) {
+                if (rc + hist[bin] >= K) { hitbin = bin; break; }
+                rc += hist[bin];
+              }
+              b_k = warp_min_i(hitbin);
+              if (b_k >= nb) b_k = 0;  // cannot happen when tot_c >= K; keeps indices in range
+              const int owner = __ffs(__ballot_sync(kFull, hitbin == b_k)) - 1;
+              unsigned long long rw = base_w;
+              unsigned rc2 = base_c;
+              if (lane == owner)
+                for (int bin = b_lo; bin < min(b_k, b_hi); ++bin) {
+                  rc2 += hist[bin];
+                  rw += (unsigned long long)hist[bin] * wbin[bin];
+                }
+              rc2 = __shfl_sync(kFull, rc2, owner);
+              rw = __shfl_sync(kFull, rw, owner);
+              jk = K - rc2;
+              s_k = rw + (unsigned long long)jk * wbin[b_k];
+              if (lane == 0) {
+                sh.sel_bcut = b_k;
+                sh.sel_jcut = jk;
+                sh.sel_kept = K;
+                sh.sel_sf = s_k;
               }
             }
-            __syncthreads();
+          }
+          if (ok && topp_on) {
+            const unsigned long long tau = (unsigned long long)ceil(
+                (double)job.top_p * (topk_on ? (double)s_k : s_total * tau_scale));
+            int hitbin = INT_MAX;
+            unsigned long long rw = base_w;
+            for (int bin = b_lo; bin < b_hi && bin <= b_k; ++bin) {
+              const unsigned cnt = (bin == b_k) ? jk : hist[bin];
+              const unsigned long long wsum = (unsigned long long)cnt * wbin[bin];
+              if (cnt && rw + wsum >= tau) { hitbin = bin; break; }
+              rw += wsum;
+            }
+            const int b_p = warp_min_i(hitbin);
+            if (b_p == INT_MAX) {
+              ok = 0;  // the window holds too little mass
+            } else {
+              const int owner = __ffs(__ballot_sync(kFull, hitbin == b_p)) - 1;
+              unsigned rc = base_c;
+              unsigned long long rw2 = base_w;
+              if (lane == owner)
+                for (int bin = b_lo; bin < min(b_p, b_hi); ++bin) {
+                  rc += hist[bin];
+                  rw2 += (unsigned long long)hist[bin] * wbin[bin];
+                }
+              rc = __shfl_sync(kFull, rc, owner);
+              rw2 = __shfl_sync(kFull, rw2, owner);
+              const unsigned avail = (b_p == b_k) ? jk : hist[b_p];
+              const unsigned long long w1 = wbin[b_p];
+              unsigned j = avail;
+              if (w1 > 0) {
+                const unsigned long long jj = (tau - rw2 + w1 - 1) / w1;
+                j = (unsigned)(jj < 1 ? 1 : (jj > avail ? avail : jj));
+              }
+              if (lane == 0) {
+                sh.sel_bcut = b_p;
+                sh.sel_jcut = j;
+                sh.sel_kept = rc + j;
+                sh.sel_sf = rw2 + (unsigned long long)j * w1;
+              }
+            }
+          }
+          if (lane == 0) {
+            sh.sel_ok = ok;
+            if (ok) {
+              sh.sel_ncut = hist[sh.sel_bcut];
+              sh.sel_cutkey = key_from16(K16m - (uint32_t)sh.sel_bcut);
+            }
+            sh.tie_n = 0;
+            sh.tie_idx = (sh.sel_ok && sh.sel_jcut == sh.sel_ncut) ? -1 : INT_MAX;
           }
         }
-        // inclusive prefix of fixed-point masses over the sorted window
-        constexpr int C = kSortCap / NT;
-        const unsigned lo = threadIdx.x * C;
-        unsigned long long run = 0;
-#pragma unroll
-        for (int t = 0; t < C; ++t) {
-          const unsigned i = lo + t;
-          if (i < n_c) run += to_fixed(tempered_weight(key_value((uint32_t)(keys[i] >> 32)), m, c));
-          pre[i] = run;
+        csync();
+        if (sh.sel_ok) {
+          const uint32_t ck16 = sh.sel_cutkey >> 16;
+          const unsigned jc = sh.sel_jcut, nc = sh.sel_ncut;
+          if (jc == nc) {
+            // the whole group of the cut key is kept: the cut is its largest index
+            const int n_own = min((int)sh.wcnt[warp], CAPW);
+            for (int i = lane; i < n_own; i += 32) {
+              const uint32_t e = region[i];
+              if (floor16 + (e & (kHistBins - 1)) == ck16) atomicMax(&sh.tie_idx, (int)(e >> kKeySpanBits));
+            }
+            csync();
+          } else if (nc <= (unsigned)kTieCap) {
+            // the jc-th member of the cut key in index order: rank the members
+            const int n_own = min((int)sh.wcnt[warp], CAPW);
+            for (int i = lane; i < n_own; i += 32) {
+              const uint32_t e = region[i];
+              if (floor16 + (e & (kHistBins - 1)) == ck16) {
+                const unsigned pos = atomicAdd(&sh.tie_n, 1u);
+                if (pos < (unsigned)kTieCap) ties[pos] = e >> kKeySpanBits;
+              }
+            }
+            csync();
+            const unsigned nt = min(sh.tie_n, (unsigned)kTieCap);
+            for (unsigned i = threadIdx.x; i < nt; i += NT) {
+              const unsigned me = ties[i];
+              unsigned rank = 0;
+              for (unsigned t = 0; t < nt; ++t) rank += (ties[t] < me);
+              if (rank + 1 == jc) sh.tie_idx = (int)me;
+            }
+            csync();
+          } else if (threadIdx.x == 0) {
+            sh.sel_ok = 0;
+          }
+          csync();
+          if (sh.sel_ok) {
+            done = true;
+            cut_key = sh.sel_cutkey;
+            cut_idx = sh.tie_idx;
+            kept = sh.sel_kept;
+            sf_fixed = sh.sel_sf;
+          }
         }
-        unsigned bc, tc;
-        unsigned long long bw, tw;
-        block_exscan(0u, run, bc, bw, tc, tw, sh);
+        csync();
+      }
+    } else {
+      if (window_ok) {
+        // ---- fp32 window: sorted by (key desc, index asc) ----
+        if (threadIdx.x == 0) sh.n_keep = 0;
+        csync();
+        {
+          const int n_own = min((int)sh.wcnt[warp], CAPW);
+          for (int i = lane; i < n_own; i += 32) {
+            const uint2 e = region[i];
+            const float z = __uint_as_float(e.y);
+            if (z >= thr) {
+              const unsigned pos = atomicAdd(&sh.n_keep, 1u);
+              if (pos < (unsigned)kSortCap)
+                keys[pos] = ((unsigned long long)order_key(z) << 32) | (unsigned long long)(~e.x);
+            }
+          }
+        }
+        csync();
+        const unsigned n_c = sh.n_keep;
+        if (n_c >= 1 && n_c <= (unsigned)kSortCap && (!topk_on || n_c >= K)) {
+          unsigned n_pad = 2;
+          while (n_pad < n_c) n_pad <<= 1;
+          for (unsigned i = n_c + threadIdx.x; i < n_pad; i += NT) keys[i] = 0ull;
+          csync();
+          for (unsigned k = 2; k <= n_pad; k <<= 1) {  // bitonic sort, descending
+            for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
+              for (unsigned i = threadIdx.x; i < n_pad; i += NT) {
+                const unsigned ixj = i ^ jj;
+                if (ixj > i) {
+                  const unsigned long long a = keys[i], b = keys[ixj];
+                  const bool swap = ((i & k) == 0) ? (a < b) : (a > b);
+                  if (swap) { keys[i] = b; keys[ixj] = a; }
+                }
+              }
+              csync();
+            }
+          }
+          // inclusive prefix of fixed-point masses over the sorted window
+          constexpr int C = kSortCap / NT;
+          const unsigned lo = threadIdx.x * C;
+          unsigned long long run = 0;
 #pragma unroll
-        for (int t = 0; t < C; ++t) pre[lo + t] += bw;
-        if (threadIdx.x == 0) sh.first = INT_MAX;
-        __syncthreads();
-        const unsigned K_eff = topk_on ? K : n_c;
-        bool ok = true;
-        unsigned cut_pos = K_eff - 1;
-        if (topp_on) {
-          const unsigned long long tau = (unsigned long long)ceil(
-              (double)job.top_p * (topk_on ? (double)pre[K - 1] : s_total * tau_scale));
-          int fj = INT_MAX;
           for (int t = 0; t < C; ++t) {
             const unsigned i = lo + t;
-            if (i < K_eff && pre[i] >= tau) { fj = (int)i; break; }
+            if (i < n_c) run += to_fixed(tempered_weight(key_value((uint32_t)(keys[i] >> 32)), m, c));
+            pre[i] = run;
           }
-          fj = warp_min_i(fj);
-          if (lane == 0 && fj != INT_MAX) atomicMin(&sh.first, fj);
-          __syncthreads();
-          if (sh.first == INT_MAX) ok = false;  // the window holds too little mass
-          else cut_pos = (unsigned)sh.first;
+          unsigned bc, tc;
+          unsigned long long bw, tw;
+          block_exscan(0u, run, bc, bw, tc, tw, sh);
+#pragma unroll
+          for (int t = 0; t < C; ++t) pre[lo + t] += bw;
+          if (threadIdx.x == 0) sh.first = INT_MAX;
+          csync();
+          const unsigned K_eff = topk_on ? K : n_c;
+          bool ok = true;
+          unsigned cut_pos = K_eff - 1;
+          if (topp_on) {
+            const unsigned long long tau = (unsigned long long)ceil(
+                (double)job.top_p * (topk_on ? (double)pre[K - 1] : s_total * tau_scale));
+            int fj = INT_MAX;
+            for (int t = 0; t < C; ++t) {
+              const unsigned i = lo + t;
+              if (i < K_eff && pre[i] >= tau) { fj = (int)i; break; }
+            }
+            fj = warp_min_i(fj);
+            if (lane == 0 && fj != INT_MAX) atomicMin(&sh.first, fj);
+            csync();
+            if (sh.first == INT_MAX) ok = false;  // the window holds too little mass
+            else cut_pos = (unsigned)sh.first;
+          }
+          if (ok) {
+            const unsigned long long kk = keys[cut_pos];
+            cut_key = (uint32_t)(kk >> 32);
+            cut_idx = (int)(~(uint32_t)kk);
+            kept = cut_pos + 1;
+            sf_fixed = pre[cut_pos];
+            done = true;
+          }
         }
-        if (ok) {
-          const unsigned long long kk = keys[cut_pos];
-          cut_key = (uint32_t)(kk >> 32);
-          cut_idx = (int)(~(uint32_t)kk);
-          kept = cut_pos + 1;
-          sf_fixed = pre[cut_pos];
-          done = true;
-        }
+        csync();
       }
-      __syncthreads();
     }
     if (!done) {
       // exact full-row selection
@@ -755,13 +1109,13 @@ __global__ void __launch_bounds__(NT, kRowBlocksPerSm) row_pass_kernel(RowJob jo
       st.kept = (int)kept;
       *out = st;
     }
-    __syncthreads();
+    csync();
   }
 }
 
 template <typename T, int MODE>
 cudaError_t launch_mode(const RowJob& job, int num_rows, cudaStream_t s) {
-  const size_t dyn = (MODE == 2) ? kDynSmem : 0;
+  const size_t dyn = row_dyn_smem<T>();
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -772,10 +1126,10 @@ cudaError_t launch_mode(const RowJob& job, int num_rows, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  int grid = device_sm_count() * kRowBlocksPerSm;
+  int grid = device_sm_count() * kRowBlocksPerSm;  // persistent blocks
   if (grid > num_rows) grid = num_rows;
   if (grid < 1) grid = 1;
-  row_pass_kernel<T, MODE><<<grid, NT, dyn, s>>>(job);
+  row_pass_kernel<T, MODE><<<grid, kBlockThreads, dyn, s>>>(job);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// walk.cu -- tree preparation and the per-tree accept walk.
+// walk.cu -- the per-tree accept walk.
 //
 // Multi-round speculative sampling on a tree (EAGLE / EAGLE-2 translation,
 // modelers.csdn.net, sections 1.3.2 and 1.7; "LLM speculative decoding: EAGLE",
@@ -10,6 +10,10 @@
 // inverse CDF.  At temperature 0 the first child whose token is the target
 // argmax is accepted and the final token is the argmax ("EAGLE close reading",
 // edgeai1.github.io, sections 3 and 5).
+//
+// One block per tree.  The block first checks the tree and builds its child
+// lists in shared memory; the walk itself is sequential, and every rejection or
+// final draw is one block-wide pass over the (p_u, q_u) row pair.
 #include <climits>
 
 #include "common.cuh"
@@ -20,58 +24,14 @@ namespace {
 
 constexpr int WT = kWalkThreads;
 constexpr int WW = WT / 32;
+constexpr int kWalkUnroll = 4;
 
 __device__ __forceinline__ const void* row_at(const void* base, const TreeJob& j, int b, int n,
                                               int bytes) {
-  int64_t off = (int64_t)b * j.batch_stride + (int64_t)n * j.row_pitch;
+  const int64_t off = (int64_t)b * j.batch_stride + (int64_t)n * j.row_pitch;
   return static_cast<const void*>(static_cast<const char*>(base) + off * bytes);
 }
 
-// ---------------------------------------------------------------------------
-// Tree preparation: one thread per tree validates parent_idx / draft_tokens,
-// builds the children lists in node order (CSR) and flags the q rows the walk
-// may need (nodes with at least one child).
-// ---------------------------------------------------------------------------
-__global__ void tree_prep_kernel(TreeJob job, int greedy) {
-  if (blockIdx.x == 0 && threadIdx.x < 8 && job.counters) job.counters[threadIdx.x] = 0ull;
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= job.B) return;
-  const int N = job.N;
-  const int32_t* par = job.parents + (int64_t)b * N;
-  const int32_t* tok = job.tokens + (int64_t)b * N;
-  int32_t* cs = job.child_start + (int64_t)b * (N + 1);
-  int32_t* cl = job.child_list + (int64_t)b * N;
-  uint8_t* nq = job.need_q + (int64_t)b * N;
-  if (job.out_alpha)
-    for (int n = 0; n < N; ++n) job.out_alpha[(int64_t)b * N + n] = __int_as_float(0x7fc00000);
-  for (int n = 0; n < N; ++n) nq[n] = 0;
-
-  int status = SPEC_TREE_OK;
-  if (par[0] != -1) status = SPEC_TREE_INVALID;
-  // depth of each node, kept in the child list until the lists are built
-  cl[0] = 0;
-  for (int n = 1; n < N && status == SPEC_TREE_OK; ++n) {
-    int p = par[n], t = tok[n];
-    if (p < 0 || p >= n || t < 0 || t >= job.V) { status = SPEC_TREE_INVALID; break; }
-    int d = cl[p] + 1;
-    if (d > job.W - 1) { status = SPEC_TREE_INVALID; break; }
-    cl[n] = d;
-  }
-  job.tree_info[b] = status;
-  if (status != SPEC_TREE_OK) return;
-  for (int u = 0; u <= N; ++u) cs[u] = 0;
-  for (int n = 1; n < N; ++n) cs[par[n] + 1] += 1;
-  for (int u = 1; u <= N; ++u) cs[u] += cs[u - 1];  // cs[u] = first slot of u's children
-  for (int n = 1; n < N; ++n) cl[cs[par[n]]++] = n; // children land in node order
-  for (int u = N; u >= 1; --u) cs[u] = cs[u - 1];
-  cs[0] = 0;
-  if (!greedy)
-    for (int u = 0; u < N; ++u) nq[u] = (cs[u + 1] > cs[u]);
-}
-
-// ---------------------------------------------------------------------------
-// Walk helpers.
-// ---------------------------------------------------------------------------
 struct WalkShared {
   double red[WW];
   double wtot[WW];
@@ -79,18 +39,20 @@ struct WalkShared {
   int target_warp;
   int accept;
   int final_tok;
+  int status;
+  float inv_sp, inv_sq;
 };
 
 // Is token x (logit z) inside the kept set of a filtered row?
 __device__ __forceinline__ bool kept_tok(float z, int x, const spec_row_stats& st) {
-  uint32_t k = order_key(z);
+  const uint32_t k = order_key(z);
   return k > st.cut_key || (k == st.cut_key && x <= st.cut_idx);
 }
 
 // Filtered probability of one token in fp64 (for the acceptance test).
 template <typename T>
 __device__ double prob64(const void* row, int x, const spec_row_stats& st, double T_) {
-  float z = Elt<T>::at(row, x);
+  const float z = Elt<T>::at(row, x);
   if (!kept_tok(z, x, st)) return 0.0;
   return exp(((double)z - (double)st.m) / T_) / st.s_f;
 }
@@ -104,17 +66,18 @@ __device__ __forceinline__ float prob32(float z, int x, const spec_row_stats& st
 // p after j renormalised residual steps: p <- max(0, p - q) / Z_r (unchanged when Z_r == 0).
 __device__ __forceinline__ float residual_chain(float p, float q, int j, const float* invz) {
   for (int r = 0; r < j; ++r) {
-    float iz = invz[r];
+    const float iz = invz[r];
     if (iz > 0.f) p = fmaxf(0.f, p - q) * iz;
   }
   return p;
 }
 
-__device__ double block_sum_d(double v, WalkShared& sh) {
+// Block sum of per-thread Kahan accumulators (float-float within warps, fp64 across).
+__device__ double block_sum(const Kahan& k, WalkShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum_d(v);
+  const FF v = warp_sum_ff(k.ff());
   __syncthreads();
-  if (lane == 0) sh.red[warp] = v;
+  if (lane == 0) sh.red[warp] = v.value();
   __syncthreads();
   double t = 0.0;
   for (int w = 0; w < WW; ++w) t += sh.red[w];
@@ -134,7 +97,7 @@ __device__ __forceinline__ void unit_values(const void* prow, const void* qrow, 
   if (j == 0) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      int x = u * E + e;
+      const int x = u * E + e;
       val[e] = (x < V) ? prob32(zp[e], x, sp, c, inv_sp) : 0.f;
     }
     return;
@@ -143,10 +106,10 @@ __device__ __forceinline__ void unit_values(const void* prow, const void* qrow, 
   load_unit<T>(qrow, V, u, zq);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    int x = u * E + e;
+    const int x = u * E + e;
     if (x < V) {
-      float p = prob32(zp[e], x, sp, c, inv_sp);
-      float q = prob32(zq[e], x, sq, c, inv_sq);
+      const float p = prob32(zp[e], x, sp, c, inv_sp);
+      const float q = prob32(zq[e], x, sq, c, inv_sq);
       val[e] = residual_chain(p, q, j, invz);
     } else {
       val[e] = 0.f;
@@ -154,10 +117,8 @@ __device__ __forceinline__ void unit_values(const void* prow, const void* qrow, 
   }
 }
 
-// Z = sum_x max(0, p^(j)(x) - q(x)) over the row pair (block-wide, fp64 result).
-// Each thread issues the loads of kWalkUnroll units of both rows before using them.
-constexpr int kWalkUnroll = 2;
-
+// Z = sum_x max(0, p^(j)(x) - q(x)) over the row pair (block-wide).  Each thread
+// issues the loads of kWalkUnroll units of both rows before using them.
 template <typename T>
 __device__ double residual_mass(const void* prow, const void* qrow, int V,
                                 const spec_row_stats& sp, const spec_row_stats& sq, float c,
@@ -194,14 +155,9 @@ __device__ double residual_mass(const void* prow, const void* qrow, int V,
     }
     acc.add(part);
   }
-  return block_sum_d(acc.value(), sh);
+  return block_sum(acc, sh);
 }
 
-// Inverse-CDF draw in index order: the smallest x with C_x >= r * C_V, where C is the
-// inclusive prefix sum of the current distribution.  Warps own contiguous ranges of
-// units; a warp step covers 32 consecutive units (one per lane) and its total is a
-// butterfly sum.  The owning warp retraces its step totals in the same order in the
-// second phase, so its running sum reproduces the first phase exactly.
 template <typename T>
 __device__ __forceinline__ float unit_sum(const void* prow, const void* qrow, int V, int u,
                                           const spec_row_stats& sp, const spec_row_stats& sq,
@@ -214,6 +170,12 @@ __device__ __forceinline__ float unit_sum(const void* prow, const void* qrow, in
   return s;
 }
 
+// Inverse-CDF draw in index order: the smallest x with C_x >= r * C_V, where C is the
+// inclusive prefix sum of the current distribution.  Warps own contiguous ranges of
+// units; a warp step covers 32 consecutive units (one per lane) and its total is an
+// fp32 butterfly sum, accumulated in float-float.  The owning warp retraces its step
+// totals in the same order in the second phase, so its running sum reproduces the
+// first phase exactly.
 template <typename T>
 __device__ int inverse_cdf(const void* prow, const void* qrow, int V, const spec_row_stats& sp,
                            const spec_row_stats& sq, float c, float inv_sp, float inv_sq, int j,
@@ -223,16 +185,16 @@ __device__ int inverse_cdf(const void* prow, const void* qrow, int V, const spec
   const int nunits = (V + E - 1) / E;
   const int per_warp = (nunits + WW - 1) / WW;
   const int u_lo = warp * per_warp, u_hi = min(nunits, u_lo + per_warp);
-  double wt = 0.0;
+  FF wt;
   for (int ub = u_lo; ub < u_hi; ub += 64) {
     float val0[E], val1[E];
-    const int ua = ub + lane, ubb = ub + 32 + lane;
+    const int ua = ub + lane, uc = ub + 32 + lane;
     const float s0 = (ua < u_hi) ? unit_sum<T>(prow, qrow, V, ua, sp, sq, c, inv_sp, inv_sq, j, invz, val0) : 0.f;
-    const float s1 = (ubb < u_hi) ? unit_sum<T>(prow, qrow, V, ubb, sp, sq, c, inv_sp, inv_sq, j, invz, val1) : 0.f;
-    wt += warp_sum_d((double)s0);
-    wt += warp_sum_d((double)s1);
+    const float s1 = (uc < u_hi) ? unit_sum<T>(prow, qrow, V, uc, sp, sq, c, inv_sp, inv_sq, j, invz, val1) : 0.f;
+    wt.add(warp_sum_f(s0));
+    wt.add(warp_sum_f(s1));
   }
-  if (lane == 0) sh.wtot[warp] = wt;
+  if (lane == 0) sh.wtot[warp] = wt.value();
   __syncthreads();
   if (threadIdx.x == 0) {
     double total = 0.0;
@@ -248,31 +210,39 @@ __device__ int inverse_cdf(const void* prow, const void* qrow, int V, const spec
       }
       cum += sh.wtot[w];
     }
-    if (tw < 0) { tw = last; tw_base = last_base; t = last_base + sh.wtot[last]; }
+    if (tw < 0 && last >= 0) { tw = last; tw_base = last_base; t = last_base + sh.wtot[last]; }
+    // an all-zero distribution (not reachable from a valid row) draws nothing: the
+    // caller falls back to the row's argmax
     sh.target_warp = tw;
-    sh.target = fmin(t - tw_base, sh.wtot[tw]);
+    sh.target = tw >= 0 ? fmin(t - tw_base, sh.wtot[tw]) : 0.0;
     sh.final_tok = -1;
   }
   __syncthreads();
   if (warp == sh.target_warp) {
     const double target = sh.target;
-    double cum = 0.0;
+    FF cum;
     bool found = false;
     for (int ub = u_lo; ub < u_hi && !found; ub += 32) {
-      // same unit order and butterfly totals as the first phase (two 32-unit steps per 64)
       const int u = ub + lane;
       float val[E];
       const float s = (u < u_hi) ? unit_sum<T>(prow, qrow, V, u, sp, sq, c, inv_sp, inv_sq, j, invz, val) : 0.f;
-      const double it = warp_sum_d((double)s);
-      if (it > 0.0 && cum + it >= target) {
-        double incl = (double)s;
+      const float it = warp_sum_f(s);
+      FF next = cum;
+      next.add(it);
+      // the crossing test is made once (lane 0) in fp64 and broadcast
+      int cross = 0;
+      if (lane == 0) cross = (it > 0.f && next.value() >= target);
+      cross = __shfl_sync(kFull, cross, 0);
+      if (cross) {
+        float incl = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double t = __shfl_up_sync(kFull, incl, o);
+          const float t = __shfl_up_sync(kFull, incl, o);
           if (lane >= o) incl += t;
         }
-        const double before = cum + incl - (double)s;
-        const unsigned hit = __ballot_sync(kFull, s > 0.f && cum + incl >= target);
+        const double base = cum.value();
+        const double before = base + (double)(incl - s);
+        const unsigned hit = __ballot_sync(kFull, s > 0.f && base + (double)incl >= target);
         const unsigned pos = __ballot_sync(kFull, s > 0.f);
         const int L = hit ? (__ffs(hit) - 1) : (31 - __clz(pos));
         int tok = -1;
@@ -293,7 +263,7 @@ __device__ int inverse_cdf(const void* prow, const void* qrow, int V, const spec
         if (lane == 0) sh.final_tok = tok;
         found = true;
       }
-      cum += it;
+      cum = next;
     }
   }
   __syncthreads();
@@ -304,31 +274,69 @@ __device__ int inverse_cdf(const void* prow, const void* qrow, int V, const spec
 // The walk: one block per tree.
 // ---------------------------------------------------------------------------
 template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(WT) tree_walk_kernel(TreeJob job) {
+__global__ void __launch_bounds__(WT, 1) tree_walk_kernel(TreeJob job) {
   __shared__ WalkShared sh;
+  // parents [N], tokens [N], child_start [N+1], children [N], then Z [N] (fp64) and 1/Z [N]
+  extern __shared__ __align__(16) int32_t tsm[];
   const int b = blockIdx.x;
   const int N = job.N, V = job.V, W = job.W;
+  int32_t* par = tsm;
+  int32_t* tok = tsm + N;
+  int32_t* cs = tsm + 2 * N;
+  int32_t* cl = tsm + 3 * N + 1;
   int32_t* out_tok = job.out_tokens + (int64_t)b * W;
   int32_t* out_path = job.out_path + (int64_t)b * W;
-  int status = job.tree_info[b];
-  double* Z = job.resid_z + (int64_t)b * N;
-  float* invz = job.resid_invz + (int64_t)b * N;
-  const int32_t* cs = job.child_start + (int64_t)b * (N + 1);
-  const int32_t* cl = job.child_list + (int64_t)b * N;
-  const int32_t* tok = job.tokens + (int64_t)b * N;
+  double* Z = reinterpret_cast<double*>(tsm + ((4 * N + 1 + 1) & ~1));
+  float* invz = reinterpret_cast<float*>(Z + N);
   const double Td = (double)job.temperature;
   const float c = job.c;
+
+  // ---- tree checks and child lists ----
+  for (int n = threadIdx.x; n < N; n += WT) {
+    par[n] = job.parents[(int64_t)b * N + n];
+    tok[n] = job.tokens[(int64_t)b * N + n];
+    if (job.out_alpha) job.out_alpha[(int64_t)b * N + n] = __int_as_float(0x7fc00000);
+  }
+  __syncthreads();
+  int bad = 0;
+  for (int n = threadIdx.x; n < N; n += WT) {
+    if (n == 0) bad |= (par[0] != -1);
+    else bad |= (par[n] < 0 || par[n] >= n || tok[n] < 0 || tok[n] >= V);
+  }
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    int status = bad ? SPEC_TREE_INVALID : SPEC_TREE_OK;
+    if (!bad) {
+      // depths (kept in the child array until the lists are built) and the depth limit
+      cl[0] = 0;
+      for (int n = 1; n < N; ++n) {
+        cl[n] = cl[par[n]] + 1;
+        if (cl[n] > W - 1) { status = SPEC_TREE_INVALID; break; }
+      }
+    }
+    if (status == SPEC_TREE_OK) {
+      for (int u = 0; u <= N; ++u) cs[u] = 0;
+      for (int n = 1; n < N; ++n) cs[par[n] + 1] += 1;
+      for (int u = 1; u <= N; ++u) cs[u] += cs[u - 1];
+      for (int n = 1; n < N; ++n) cl[cs[par[n]]++] = n;  // children land in node order
+      for (int u = N; u >= 1; --u) cs[u] = cs[u - 1];
+      cs[0] = 0;
+    }
+    sh.status = status;
+  }
+  __syncthreads();
+  int status = sh.status;
 
   int u = 0, n_acc = 0, final_tok = -1;
   while (status == SPEC_TREE_OK) {
     const spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
-    if (sp.status != SPEC_TREE_OK) { status = SPEC_ROW_NONFINITE; break; }
+    if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
     const int c0 = cs[u], c1 = cs[u + 1];
     if (GREEDY) {
       int next = -1;
       for (int i = c0; i < c1; ++i) {
-        int ch = cl[i];
-        bool ok = tok[ch] == sp.argmax;
+        const int ch = cl[i];
+        const bool ok = tok[ch] == sp.argmax;
         if (threadIdx.x == 0 && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = ok ? 1.f : 0.f;
         if (ok) { next = ch; break; }
       }
@@ -349,30 +357,34 @@ __global__ void __launch_bounds__(WT) tree_walk_kernel(TreeJob job) {
     spec_row_stats sq = sp;
     if (c1 > c0) {
       sq = job.stats_q[(int64_t)b * N + u];
-      if (sq.status != SPEC_TREE_OK) { status = SPEC_ROW_NONFINITE; break; }
+      if (sq.status != SPEC_TREE_OK) { status = sq.status; break; }
     }
-    const float inv_sp = (float)(1.0 / sp.s_f);
-    const float inv_sq = (float)(1.0 / sq.s_f);
+    if (threadIdx.x == 0) {
+      sh.inv_sp = (float)(1.0 / sp.s_f);
+      sh.inv_sq = (float)(1.0 / sq.s_f);
+    }
+    __syncthreads();
+    const float inv_sp = sh.inv_sp, inv_sq = sh.inv_sq;
     int j = 0, next = -1;
     for (int i = c0; i < c1; ++i) {
       const int ch = cl[i];
       if (threadIdx.x == 0) {
         const int x = tok[ch];
         double P = prob64<T>(prow, x, sp, Td);
-        double Q = prob64<T>(qrow, x, sq, Td);
+        const double Q = prob64<T>(qrow, x, sq, Td);
         for (int r = 0; r < j; ++r)
           if (Z[r] > 0.0) P = fmax(0.0, P - Q) / Z[r];
-        double alpha = (Q > 0.0) ? fmin(1.0, P / Q) : (P > 0.0 ? 1.0 : 0.0);
-        uint4 w = philox_words(job.seed, job.offset, b, ch);
-        double r = unit_uniform(w.x);
+        const double alpha = (Q > 0.0) ? fmin(1.0, P / Q) : (P > 0.0 ? 1.0 : 0.0);
+        const uint4 w = philox_words(job.seed, job.offset, b, ch);
+        const double rr = unit_uniform(w.x);
         if (job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = (float)alpha;
-        sh.accept = (r <= alpha);
+        sh.accept = (rr <= alpha);
       }
       __syncthreads();
       const int acc = sh.accept;
       __syncthreads();
       if (acc) { next = ch; break; }
-      double z = residual_mass<T>(prow, qrow, V, sp, sq, c, inv_sp, inv_sq, j, invz, sh);
+      const double z = residual_mass<T>(prow, qrow, V, sp, sq, c, inv_sp, inv_sq, j, invz, sh);
       if (threadIdx.x == 0) {
         Z[j] = z;
         invz[j] = (z > 0.0) ? (float)(1.0 / z) : -1.f;
@@ -393,9 +405,10 @@ __global__ void __launch_bounds__(WT) tree_walk_kernel(TreeJob job) {
       u = next;
       continue;
     }
-    uint4 w = philox_words(job.seed, job.offset, b, u);
-    double r = unit_uniform(w.y);
-    final_tok = inverse_cdf<T>(prow, qrow, V, sp, sq, c, inv_sp, inv_sq, j, invz, r, sh);
+    const uint4 w = philox_words(job.seed, job.offset, b, u);
+    const double rr = unit_uniform(w.y);
+    final_tok = inverse_cdf<T>(prow, qrow, V, sp, sq, c, inv_sp, inv_sq, j, invz, rr, sh);
+    if (final_tok < 0) final_tok = sp.argmax;
     if (threadIdx.x == 0 && job.counters) {
       atomicAdd(&job.counters[2], (unsigned long long)(j > 0 ? 2 : 1) * V * Elt<T>::kBytes);
       atomicAdd(&job.counters[4], 1ull);
@@ -418,32 +431,31 @@ __global__ void __launch_bounds__(WT) tree_walk_kernel(TreeJob job) {
 
 __global__ void philox_words_kernel(uint64_t seed, uint64_t offset, const int32_t* b_idx,
                                     const int32_t* node_idx, int32_t n, uint32_t* out) {
-  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  uint4 w = philox_words(seed, offset, b_idx[i], node_idx[i]);
+  const uint4 w = philox_words(seed, offset, b_idx[i], node_idx[i]);
   reinterpret_cast<uint4*>(out)[i] = w;
+}
+
+template <typename T, bool GREEDY>
+cudaError_t launch_walk_t(const TreeJob& job, cudaStream_t s) {
+  const size_t dyn = (size_t)((4 * job.N + 1 + 1) & ~1) * sizeof(int32_t) +
+                     (size_t)job.N * (sizeof(double) + sizeof(float));
+  if (dyn > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        tree_walk_kernel<T, GREEDY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+  }
+  tree_walk_kernel<T, GREEDY><<<job.B, WT, dyn, s>>>(job);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_tree_prep(const TreeJob& job, bool greedy, cudaStream_t s) {
-  const int threads = 64;
-  int blocks = (job.B + threads - 1) / threads;
-  if (blocks < 1) blocks = 1;
-  tree_prep_kernel<<<blocks, threads, 0, s>>>(job, greedy ? 1 : 0);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, cudaStream_t s) {
-  dim3 grid(job.B);
-  if (dtype == SPEC_BF16) {
-    if (greedy) tree_walk_kernel<uint16_t, true><<<grid, WT, 0, s>>>(job);
-    else tree_walk_kernel<uint16_t, false><<<grid, WT, 0, s>>>(job);
-  } else {
-    if (greedy) tree_walk_kernel<float, true><<<grid, WT, 0, s>>>(job);
-    else tree_walk_kernel<float, false><<<grid, WT, 0, s>>>(job);
-  }
-  return cudaGetLastError();
+  if (dtype == SPEC_BF16)
+    return greedy ? launch_walk_t<uint16_t, true>(job, s) : launch_walk_t<uint16_t, false>(job, s);
+  return greedy ? launch_walk_t<float, true>(job, s) : launch_walk_t<float, false>(job, s);
 }
 
 cudaError_t launch_philox_words(uint64_t seed, uint64_t offset, const int32_t* b_idx,

@@ -137,6 +137,26 @@ def test_filter_rows_non_finite():
         assert list(s) == [1, 1, 1, 0, 0], (T, k, p, s)
 
 
+def test_bounded_wait_self_test_reports_timeout():
+    """The stall self-test withholds one copy's completion: the row pass's bounded
+    wait gives up, the rows report SPEC_ROW_TIMEOUT, and the next call is normal."""
+    x = _rows("gauss", 8, 40000, torch.bfloat16, seed=1)
+    for T, k, p in ((0.7, 0, 0.9), (1.0, 0, 1.0), (0.0, 0, 1.0)):
+        st = binding.filter_rows(_dev_rows(x), T, k, p, binding.SPEC_FLAG_TEST_STALL)
+        torch.cuda.synchronize()
+        assert (st["status"].cpu().numpy() == binding.SPEC_ROW_TIMEOUT).all()
+        st = binding.filter_rows(_dev_rows(x), T, k, p)
+        torch.cuda.synchronize()
+        assert (st["status"].cpu().numpy() == 0).all()
+    w = W["tree60_b64_v128256"].with_(B=4, V=40000)
+    inp = gpu_inputs(w, 2)
+    out = run_gpu(w, inp, flags=binding.SPEC_FLAG_TEST_STALL)
+    assert (out["status"] == binding.SPEC_ROW_TIMEOUT).all()
+    assert (out["accept_len"] == -1).all()
+    out = run_gpu(w, inp)
+    assert (out["status"] == 0).all()
+
+
 def test_filter_rows_negative_zero_ties():
     x = torch.tensor([[-0.0, 0.0, -1.0, -0.0, -3.0]])
     st = binding.filter_rows(_dev_rows(x), 1.0, 2, 1.0)

@@ -18,7 +18,8 @@
  *
  * Conventions shared by every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller, unless stated.
- *     The library allocates nothing and keeps no state between calls.
+ *     The library allocates nothing and keeps no state between calls, apart from
+ *     the scratch address that spec_verify_tree_noalloc caches per device.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *     and returns before the GPU work finishes; it never synchronises the device.
  *   - The return value is SPEC_OK (0) or a negative SPEC_ERR_* code.  Argument
@@ -161,6 +162,44 @@ int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtyp
                      int32_t* out_accept_len, int32_t* out_tokens, int32_t* out_accepted_path,
                      float* out_alpha, int32_t* out_status, spec_verify_counters* out_counters,
                      void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Bytes of the library's own scratch behind spec_verify_tree_noalloc (one copy per
+ * device).  With the current workspace layout it holds B * N <= 16376 nodes. */
+#define SPEC_STATIC_WORKSPACE_BYTES (1u << 20)
+
+/*
+ * spec_verify_tree without a caller workspace and without allocating anything.
+ * The method's pages have no counterpart of this call; it exists for callers that
+ * must not allocate device memory during a step: cudaMalloc / cudaFree can
+ * synchronise the whole device and stall other streams, which a decode loop under
+ * a latency budget cannot afford, and a program whose memory pool owns all device
+ * memory may forbid allocations it did not make.
+ *
+ * Arguments, outputs and results are those of spec_verify_tree, minus workspace
+ * and workspace_bytes: the scratch is a fixed SPEC_STATIC_WORKSPACE_BYTES array
+ * inside this library, one per device, reserved when the library's device code is
+ * loaded.  Nothing in it needs to start at zero (the call resets what it reads).
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * scratch's device address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture begins.  Later calls only launch.
+ * Sharing: all calls on one device use the same scratch.  Two calls whose GPU work
+ * may overlap (different streams without an ordering event, or concurrent host
+ * threads on different streams) race on it and give undefined results; order them
+ * on one stream or with events.
+ * Errors: as spec_verify_tree; trees too large for the scratch (the workspace that
+ * spec_verify_workspace_size reports exceeds SPEC_STATIC_WORKSPACE_BYTES) return
+ * SPEC_ERR_TOO_LARGE before anything touches the device; a failed address lookup
+ * returns SPEC_ERR_CUDA.
+ */
+int spec_verify_tree_noalloc(const void* logits_p, const void* logits_q, spec_dtype dtype,
+                             int32_t B, int32_t N, int32_t V, int64_t row_pitch,
+                             int64_t batch_stride, const int32_t* draft_tokens,
+                             const int32_t* parent_idx, int32_t max_depth,
+                             spec_sampling_params params, uint64_t rng_seed, uint64_t rng_offset,
+                             int32_t* out_accept_len, int32_t* out_tokens,
+                             int32_t* out_accepted_path, float* out_alpha, int32_t* out_status,
+                             spec_verify_counters* out_counters, spec_stream_t stream);
 
 /* Phases of one verify call, for spec_verify_tree_phases. */
 #define SPEC_PHASE_PREPARE 1u /* reset the work counters (when out_counters is requested) */

@@ -32,6 +32,7 @@ SPEC_PHASE_WALK = 4
 SPEC_PHASE_ALL = 7
 SPEC_MAX_NODES = 4096
 SPEC_MAX_VOCAB = 1 << 21
+SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
 ERRORS = {0: "SPEC_OK", -1: "SPEC_ERR_INVALID_ARG", -2: "SPEC_ERR_UNSUPPORTED_DTYPE",
           -3: "SPEC_ERR_MISALIGNED", -4: "SPEC_ERR_WORKSPACE", -5: "SPEC_ERR_CUDA",
           -6: "SPEC_ERR_TOO_LARGE"}
@@ -81,6 +82,8 @@ def lib():
             L.spec_verify_tree.restype = ctypes.c_int
             L.spec_verify_tree_phases.argtypes = [ctypes.c_uint32] + L.spec_verify_tree.argtypes
             L.spec_verify_tree_phases.restype = ctypes.c_int
+            L.spec_verify_tree_noalloc.argtypes = L.spec_verify_tree.argtypes[:20] + [P]
+            L.spec_verify_tree_noalloc.restype = ctypes.c_int
             L.spec_filter_rows.argtypes = [P, ctypes.c_int, i32, i32, i64, SamplingParams, P, P]
             L.spec_filter_rows.restype = ctypes.c_int
             L.spec_philox_words.argtypes = [u64, u64, P, P, i32, P, P]
@@ -181,6 +184,41 @@ def verify_tree(p: torch.Tensor, q, draft_tokens: torch.Tensor, parent_idx: torc
         c = counters.cpu().numpy().view("uint64")
         out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
                                     "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))
+    return out
+
+
+def verify_tree_noalloc(p: torch.Tensor, q, draft_tokens: torch.Tensor, parent_idx: torch.Tensor,
+                        max_depth: int, temperature: float, top_k: int = 0, top_p: float = 1.0,
+                        seed: int = 0, offset: int = 0, flags: int = 0, *,
+                        batch_broadcast: bool = False, out: dict, counters=None, stream=None):
+    """spec_verify_tree_noalloc on device tensors: the library's own scratch stands in
+    for the workspace.  `out` holds caller-allocated device tensors accept_len [B],
+    tokens [B, D+1], path [B, D+1], status [B] and optionally alpha [B, N];
+    `counters` is an optional int64 device tensor of 8 entries.  This wrapper
+    allocates nothing either."""
+    B, N = draft_tokens.shape
+    V = p.shape[-1]
+    if draft_tokens.dtype != torch.int32 or parent_idx.dtype != torch.int32:
+        raise TypeError("draft_tokens and parent_idx must be int32")
+    if not (draft_tokens.is_contiguous() and parent_idx.is_contiguous()):
+        raise ValueError("draft_tokens and parent_idx must be contiguous")
+    dt = _dtype_code(p)
+    pitch, bstride = _row_layout(p, B, N, V, batch_broadcast)
+    if q is not None:
+        if q.dtype != p.dtype:
+            raise TypeError("p and q logits must share a dtype")
+        if _row_layout(q, B, N, V, batch_broadcast) != (pitch, bstride):
+            raise ValueError("p and q must share one layout")
+    rc = lib().spec_verify_tree_noalloc(
+        p.data_ptr(), None if q is None else q.data_ptr(), dt, B, N, V, pitch, bstride,
+        draft_tokens.data_ptr(), parent_idx.data_ptr(), int(max_depth),
+        params(temperature, top_k, top_p, flags), int(seed) & (2**64 - 1),
+        int(offset) & (2**64 - 1), out["accept_len"].data_ptr(), out["tokens"].data_ptr(),
+        out["path"].data_ptr(), out["alpha"].data_ptr() if "alpha" in out else None,
+        out["status"].data_ptr(), None if counters is None else counters.data_ptr(),
+        _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_verify_tree_noalloc")
     return out
 
 

@@ -20,7 +20,9 @@ constexpr int kKeySpanBits = 11;   // bf16 entries: key offset above the row's f
 constexpr int kSortCap = 2048;     // largest window resolved by sorting (fp32 rows)
 constexpr int kHistBins = 1 << kKeySpanBits;  // one bin per bf16 key below the row maximum
 constexpr int kTieCap = 1024;      // largest group of equal logits cut by index ranking
-constexpr int kWalkThreads = 512;  // threads of one tree-walk block
+constexpr int kWalkThreads = 128;         // threads of one greedy tree-walk block
+constexpr int kClusterWalkThreads = 256;  // threads of one CTA of a sampling tree-walk cluster
+constexpr int kMaxWalkCluster = 8;        // CTAs that share one tree in the sampling walk
 // Width of the single-pass candidate window below the running row maximum, in
 // nats of the tempered distribution (tokens further below carry < e^-9 of the top
 // token's weight each).  When the window misses the top-k / top-p cut, or holds

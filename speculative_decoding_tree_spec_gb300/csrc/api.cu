@@ -121,6 +121,11 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   tj.stats_q = stats_q;
   tj.temperature = params.temperature;
   tj.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)params.temperature);
+  tj.top_k = (params.top_k > 0 && params.top_k < V) ? params.top_k : 0;
+  tj.top_p = params.top_p >= 1.0f ? 1.0f : params.top_p;
+  tj.trunc = (!greedy && (tj.top_k > 0 || tj.top_p < 1.0f)) ? 1 : 0;
+  tj.delta_z = kWindowNats * params.temperature;
+  tj.exact = (params.flags & SPEC_FLAG_EXACT_SELECT) ? 1 : 0;
   tj.seed = rng_seed;
   tj.offset = rng_offset;
   tj.out_accept_len = out_accept_len;
@@ -144,6 +149,9 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   rj.B = B;
   rj.mode = kRowsTree;
   rj.with_q = greedy ? 0 : 1;
+  // the row pass supplies max, sum and argmax only; the walk cuts the rows it visits
+  rj.top_k = 0;
+  rj.top_p = 1.0f;
   rj.parents = parent_idx;
   rj.stats_p = stats_p;
   rj.stats_q = stats_q;

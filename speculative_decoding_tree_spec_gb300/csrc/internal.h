@@ -86,6 +86,13 @@ struct TreeJob {
   const spec_row_stats* stats_q;
   float temperature;
   float c;
+  // top-k / top-p cut, computed by the walk for the rows it visits (the row pass
+  // then supplies only max, sum and argmax): trunc = a cut is needed
+  int32_t trunc;
+  int32_t top_k;      // 0 = off
+  float top_p;        // 1 = off
+  float delta_z;      // candidate window below the row maximum (logit units)
+  int32_t exact;      // always take the full-row exact selection
   uint64_t seed, offset;
   int32_t* out_accept_len;
   int32_t* out_tokens;

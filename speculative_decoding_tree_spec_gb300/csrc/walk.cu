@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "select.cuh"
 
 namespace svk {
 
@@ -35,6 +36,12 @@ constexpr int CW = CT / 32;
 constexpr int kMaxC = kMaxWalkCluster;
 constexpr int kUnitsInFlight = 2;          // units of each row a thread loads before using them
 constexpr uint64_t kExchangeLimitNs = 2000000000ull;
+constexpr int kSlotW = 4;      // 64-bit words one CTA can push in one exchange
+constexpr int kCandCTA = 512;  // window candidates one CTA keeps per row
+constexpr int kSortW = 2048;   // largest window (per row) the walk resolves by sorting
+constexpr int kSortPer = kSortW / CT;
+constexpr int kWalkBins = 1024;  // bf16: one bin per key in the window below the row maximum
+static_assert(CT == kSelThreads, "the exact selection runs on one walk CTA");
 
 __device__ __forceinline__ const void* row_at(const void* base, const TreeJob& j, int b, int n,
                                               int bytes) {
@@ -319,8 +326,21 @@ __device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_peer_f64(uint32_t addr, double v) {
-  asm volatile("st.shared::cluster.f64 [%0], %1;\n" ::"r"(addr), "d"(v) : "memory");
+__device__ __forceinline__ void st_peer_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_peer_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_cluster() {
+  asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
 }
 __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_addr)
@@ -350,40 +370,73 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+typedef uint64_t SlotRow[kSlotW];
+
 struct CShared {
-  double slot[2][kMaxC];  // partials pushed by every CTA, two alternating sets
-  uint64_t xbar[2];       // one mbarrier per slot set, C arrivals per phase
+  SlotRow slot[2][kMaxC];  // words pushed by every CTA, two alternating sets
+  uint64_t xbar[2];        // one mbarrier per slot set, C arrivals per phase
   double wred[CW];
   double wtot[CW];
   double target;
   int accept, status, target_warp, final_tok;
-  unsigned err;           // rank 0: timeouts reported by any CTA of the cluster
+  unsigned err;            // rank 0: timeouts reported by any CTA of the cluster
   float inv_sp, inv_sq;
+  unsigned ncand[2];       // window candidates of this CTA's slice, per row
+  int first;
+  unsigned long long massk;
+  unsigned long long cut_w[4];
+  // bf16 window scan results, per row
+  int sc_ok[2], sc_bin[2];
+  unsigned sc_j[2], sc_kept[2], sc_ncut[2];
+  unsigned long long sc_sf[2];
+  unsigned tie_cnt[2], mem_n[2];
+  int tie_max[2], tie_idx[2];
+  SelShared sel;
 };
 
-// Cluster-wide sum of one value per CTA (`v` is read from thread 0).  Every CTA
-// pushes v into slot[set][rank] of every CTA and arrives on that CTA's mbarrier;
-// after the local mbarrier completes, each thread sums the C slots in rank order.
-// Returns false (uniformly over the CTA) if the wait gave up.  A slot set is
-// written again two exchanges later, which no CTA can start before every CTA has
-// pushed the exchange in between -- after its threads read this one.
-__device__ bool cluster_sum(double v, CShared& sh, int C, uint32_t rank, uint32_t& n_ex,
-                            double& total, const double** slots) {
+struct BSync {
+  __device__ static void sync() { __syncthreads(); }
+};
+
+// Cluster exchange: every CTA pushes nv words (thread 0's v) into slot[set][rank]
+// of every CTA and arrives on that CTA's mbarrier; once the local mbarrier
+// completes, slot[set][c] holds CTA c's words in every CTA.  Returns the slot set,
+// or nullptr (uniformly over the CTA) if the wait gave up.  Shared-memory writes
+// a CTA made before the call are visible to the other CTAs after it.  A slot set
+// is written again two exchanges later, which no CTA can start before every CTA
+// has pushed the exchange in between -- after its threads read this one.
+__device__ const SlotRow* cluster_share(const uint64_t* v, int nv, CShared& sh, int C,
+                                        uint32_t rank, uint32_t& n_ex) {
   const int set = n_ex & 1;
   const uint32_t parity = (n_ex >> 1) & 1u;
   ++n_ex;
+  __syncthreads();
   if (threadIdx.x == 0) {
+    fence_cluster();
     for (int c = 0; c < C; ++c) {
-      st_peer_f64(peer_addr(&sh.slot[set][rank], c), v);
+      for (int w = 0; w < nv; ++w) st_peer_u64(peer_addr(&sh.slot[set][rank][w], c), v[w]);
       arrive_peer(peer_addr(&sh.xbar[set], c));
     }
   }
   const bool ok = __syncthreads_and(mbar_wait_cluster(&sh.xbar[set], parity, kExchangeLimitNs));
+  return ok ? sh.slot[set] : nullptr;
+}
+
+// Cluster-wide sum of one fp64 value per CTA (read from thread 0), added in rank
+// order so that every CTA holds the same bits.
+__device__ bool cluster_sum(double v, CShared& sh, int C, uint32_t rank, uint32_t& n_ex,
+                            double& total, double* per_cta) {
+  const uint64_t w = (uint64_t)__double_as_longlong(v);
+  const SlotRow* sl = cluster_share(&w, 1, sh, C, rank, n_ex);
+  if (!sl) return false;
   double t = 0.0;
-  for (int c = 0; c < C; ++c) t += sh.slot[set][c];
+  for (int c = 0; c < C; ++c) {
+    const double x = __longlong_as_double((long long)sl[c][0]);
+    if (per_cta) per_cta[c] = x;
+    t += x;
+  }
   total = t;
-  if (slots) *slots = sh.slot[set];
-  return ok;
+  return true;
 }
 
 // Block sum of per-thread float-float partials in fixed order (result in thread 0).
@@ -489,8 +542,8 @@ __device__ int cluster_inverse_cdf(const void* prow, const void* qrow, int V, in
   if (threadIdx.x == 0)
     for (int w = 0; w < CW; ++w) v += sh.wtot[w];
   double total;
-  const double* cta_tot = nullptr;
-  ok = cluster_sum(v, sh, C, rank, n_ex, total, &cta_tot);
+  double cta_tot[kMaxC];
+  ok = cluster_sum(v, sh, C, rank, n_ex, total, cta_tot);
   owner = -1;
   if (!ok) return -1;
   double base_c = 0.0, t_c = 0.0;
@@ -564,6 +617,599 @@ __device__ int cluster_inverse_cdf(const void* prow, const void* qrow, int V, in
 }
 
 // ---------------------------------------------------------------------------
+// Top-k / top-p cut of the rows the walk visits ("LLM speculative decoding:
+// EAGLE", jingming.pro, section 1 note: p and q are compared after the sampling
+// transforms).  The row pass supplies each row's maximum m and full sum; here the
+// cluster finds (cut key, cut index, kept count, filtered sum) exactly:
+//   1. every CTA collects the tokens of its slice with logit >= m - delta_z (the
+//      candidate window) as (order key << 32 | ~index), so that a descending
+//      sort orders them by (logit desc, index asc);
+//   2. the CTAs exchange their counts, every CTA gathers all candidates through
+//      distributed shared memory, sorts them (bitonic, the same input in every
+//      CTA) and scans their exact 42-bit fixed-point masses for the top-k and
+//      top-p crossings;
+//   3. when the window cannot decide the cut (too few candidates for top-k, too
+//      little mass for top-p, or more candidates than fit), CTA 0 runs the exact
+//      full-row selection and shares its result.
+// Both routes give the same statistics the dense row pass computes for a row.
+// ---------------------------------------------------------------------------
+struct RowCut {
+  uint32_t key;
+  int idx;
+  unsigned kept;
+  uint64_t mass;  // fixed point, 2^-42
+};
+
+// Step 1 for up to two rows: candidates of units [ua, ub) go to cand[r][...];
+// with bf16 rows also one count per key in hist[r][K16m[r] - key16].
+template <typename T>
+__device__ void window_collect(const void* const (&rows)[2], int nrows, int V, int ua, int ub,
+                               const float (&thr)[2], uint64_t* const (&cand)[2],
+                               unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
+                               CShared& sh) {
+  constexpr int E = Elt<T>::kPerUnit;
+  for (int u = ua + threadIdx.x; u < ub; u += CT) {
+    uint4 raw[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (r < nrows) raw[r] = load_raw<T>(rows[r], V, u);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
+      float z[E];
+      Elt<T>::unpack(raw[r], z);
+      float mx = z[0];
+#pragma unroll
+      for (int e = 1; e < E; ++e) mx = fmaxf(mx, z[e]);
+      if (mx >= thr[r]) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (z[e] >= thr[r]) {
+            const uint32_t k = order_key(z[e]);
+            const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
+            if (pos < (unsigned)kCandCTA)
+              cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
+            if (hist[r]) {
+              const uint32_t bin = k16m[r] - (k >> 16);
+              if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// Step 2 after the sort: the cut from n sorted candidates (descending, padded to
+// n_pad with zeros), or false when the window cannot decide it.  Same rule as the
+// dense row pass's sorted window.
+__device__ bool window_cut(const uint64_t* keys, unsigned n, unsigned n_pad, float m, float c,
+                           double s_all, const TreeJob& job, CShared& sh, RowCut& out) {
+  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
+  const unsigned K = topk_on ? (unsigned)job.top_k : n;
+  const int lane = threadIdx.x & 31;
+  const unsigned lo = threadIdx.x * (unsigned)kSortPer;
+  if (threadIdx.x == 0) sh.first = INT_MAX;
+  unsigned long long pre[kSortPer];
+  unsigned long long run = 0;
+#pragma unroll
+  for (int t = 0; t < kSortPer; ++t) {
+    const unsigned i = lo + t;
+    if (i < n) run += to_fixed(tempered_weight(key_value((uint32_t)(keys[i] >> 32)), m, c));
+    pre[t] = run;
+  }
+  unsigned bc, tc;
+  unsigned long long bw, tw;
+  block_exscan<BSync>(0u, run, bc, bw, tc, tw, sh.sel);
+#pragma unroll
+  for (int t = 0; t < kSortPer; ++t) pre[t] += bw;
+  unsigned cut_pos = K - 1;
+  if (topp_on) {
+    if (topk_on && K - 1 >= lo && K - 1 < lo + kSortPer) {
+#pragma unroll
+      for (int t = 0; t < kSortPer; ++t)
+        if (lo + t == K - 1) sh.massk = pre[t];
+    }
+    __syncthreads();
+    const unsigned long long tau = (unsigned long long)ceil(
+        (double)job.top_p * (topk_on ? (double)sh.massk : s_all * 4398046511104.0));
+    int fj = INT_MAX;
+#pragma unroll
+    for (int t = 0; t < kSortPer; ++t) {
+      const unsigned i = lo + t;
+      if (fj == INT_MAX && i < K && pre[t] >= tau) fj = (int)i;
+    }
+    fj = warp_min_i(fj);
+    if (lane == 0 && fj != INT_MAX) atomicMin(&sh.first, fj);
+    __syncthreads();
+    if (sh.first == INT_MAX) return false;  // the window holds too little mass
+    cut_pos = (unsigned)sh.first;
+  }
+  if (cut_pos >= lo && cut_pos < lo + kSortPer) {
+#pragma unroll
+    for (int t = 0; t < kSortPer; ++t)
+      if (lo + t == cut_pos) {
+        sh.cut_w[0] = keys[cut_pos];
+        sh.cut_w[1] = pre[t];
+      }
+  }
+  __syncthreads();
+  out.key = (uint32_t)(sh.cut_w[0] >> 32);
+  out.idx = (int)(~(uint32_t)sh.cut_w[0]);
+  out.kept = cut_pos + 1;
+  out.mass = sh.cut_w[1];
+  __syncthreads();
+  return true;
+}
+
+// The exact selection of one row by this CTA alone (the dense row pass's rule).
+template <typename T>
+__device__ RowCut exact_cut(const void* row, int V, float m, float c, double s_all,
+                            const TreeJob& job, CShared& sh) {
+  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
+  SelOut rk{};
+  const Eligible all{false, 0u, 0};
+  if (topk_on) rk = exact_select<T, BSync>(row, V, m, c, false, (unsigned)job.top_k, 0ull, all, sh.sel);
+  RowCut out;
+  if (topp_on) {
+    const Eligible in_k{topk_on, rk.key, rk.idx};
+    const unsigned long long tau = (unsigned long long)ceil(
+        (double)job.top_p * (topk_on ? (double)rk.mass_kept : s_all * 4398046511104.0));
+    const SelOut rp = exact_select<T, BSync>(row, V, m, c, true, 0u, tau, in_k, sh.sel);
+    out.key = rp.key; out.idx = rp.idx; out.kept = rp.kept; out.mass = rp.mass_kept;
+  } else {
+    out.key = rk.key; out.idx = rk.idx; out.kept = rk.kept; out.mass = rk.mass_kept;
+  }
+  return out;
+}
+
+__device__ __forceinline__ void set_cut(spec_row_stats& s, const RowCut& rc) {
+  s.cut_key = rc.key;
+  s.cut_idx = rc.idx;
+  s.kept = (int)rc.kept;
+  s.s_f = fixed_to_double(rc.mass);
+}
+
+// The exact selection of one row on CTA 0, shared with the cluster.
+template <typename T>
+__device__ bool shared_exact_cut(const TreeJob& job, const void* row, const spec_row_stats& s,
+                                 CShared& sh, int C, uint32_t rank, uint32_t& n_ex, float c,
+                                 RowCut& rc) {
+  uint64_t w[3] = {0ull, 0ull, 0ull};
+  if (rank == 0) {
+    const RowCut ex = exact_cut<T>(row, job.V, s.m, c, s.s_f, job, sh);
+    w[0] = (uint64_t)ex.key | ((uint64_t)(uint32_t)ex.idx << 32);
+    w[1] = ex.kept;
+    w[2] = ex.mass;
+    if (threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[5], 1ull);
+  }
+  const SlotRow* x = cluster_share(w, 3, sh, C, rank, n_ex);
+  if (!x) return false;
+  rc.key = (uint32_t)x[0][0];
+  rc.idx = (int)(uint32_t)(x[0][0] >> 32);
+  rc.kept = (unsigned)x[0][1];
+  rc.mass = x[0][2];
+  return true;
+}
+
+// The cut of the p row (and of the q row when with_q) of node u, written into the
+// statistics every CTA holds (rows of any dtype: gathered window, sorted).  `cand` holds this node's two candidate lists (the
+// caller alternates between two sets from node to node, so a list is rewritten
+// only after an exchange that every CTA reaches after reading it); `sortb` the two
+// sort buffers.  Returns false if an exchange gave up.
+template <typename T>
+__device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const void* qrow,
+                                   bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
+                                   int ub, uint64_t* cand, uint64_t* sortb, CShared& sh, int C,
+                                   uint32_t rank, uint32_t& n_ex, float c) {
+  const int V = job.V;
+  const int nrows = with_q ? 2 : 1;
+  spec_row_stats* st[2] = {&sp, &sq};
+  const void* const rows[2] = {prow, qrow};
+  const float thr[2] = {sp.m - job.delta_z, sq.m - job.delta_z};
+  uint64_t* const cl[2] = {cand, cand + kCandCTA};
+  unsigned* const no_hist[2] = {nullptr, nullptr};
+  const uint32_t no_k16[2] = {0u, 0u};
+  if (threadIdx.x == 0) { sh.ncand[0] = 0u; sh.ncand[1] = 0u; }
+  __syncthreads();
+  if (!job.exact) window_collect<T>(rows, nrows, V, ua, ub, thr, cl, no_hist, no_k16, sh);
+  __syncthreads();
+  const uint64_t counts = (uint64_t)sh.ncand[0] | ((uint64_t)sh.ncand[1] << 32);
+  const SlotRow* sl = cluster_share(&counts, 1, sh, C, rank, n_ex);
+  if (!sl) return false;
+  unsigned cnt[2][kMaxC], total[2] = {0u, 0u}, n_pad[2] = {2u, 2u};
+  bool fast[2] = {false, false};
+  for (int r = 0; r < nrows; ++r) {
+    bool over = false;
+    for (int q = 0; q < C; ++q) {
+      cnt[r][q] = (unsigned)(sl[q][0] >> (32 * r));
+      over |= cnt[r][q] > (unsigned)kCandCTA;
+      total[r] += min(cnt[r][q], (unsigned)kCandCTA);
+    }
+    const bool topk_on = job.top_k > 0;
+    fast[r] = !job.exact && !over && total[r] >= 1u && total[r] <= (unsigned)kSortW &&
+              (!topk_on || total[r] >= (unsigned)job.top_k);
+    while (n_pad[r] < total[r]) n_pad[r] <<= 1;
+  }
+  // gather every CTA's candidates (remote shared memory) into the sort buffers
+  for (int r = 0; r < nrows; ++r) {
+    if (!fast[r]) continue;
+    uint64_t* keys = sortb + r * kSortW;
+    for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
+      uint64_t v = 0ull;
+      if (i < total[r]) {
+        unsigned off = 0, q = 0;
+        while (q + 1 < (unsigned)C && i >= off + cnt[r][q]) { off += cnt[r][q]; ++q; }
+        v = ld_peer_u64(peer_addr(cl[r] + (i - off), q));
+      }
+      keys[i] = v;
+    }
+  }
+  __syncthreads();
+  const unsigned pad_max = max(fast[0] ? n_pad[0] : 0u, fast[1] ? n_pad[1] : 0u);
+  for (unsigned k = 2; k <= pad_max; k <<= 1) {  // bitonic sort, descending
+    for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int r = 0; r < nrows; ++r) {
+        if (!fast[r] || k > n_pad[r]) continue;
+        uint64_t* keys = sortb + r * kSortW;
+        for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
+          const unsigned ixj = i ^ jj;
+          if (ixj > i) {
+            const uint64_t a = keys[i], b = keys[ixj];
+            const bool swap = ((i & k) == 0) ? (a < b) : (a > b);
+            if (swap) { keys[i] = b; keys[ixj] = a; }
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = 0; r < nrows; ++r) {
+    spec_row_stats& s = *st[r];
+    RowCut rc{};
+    bool ok = fast[r] && window_cut(sortb + r * kSortW, total[r], n_pad[r], s.m, c, s.s_f, job,
+                                    sh, rc);
+    if (!ok && !shared_exact_cut<T>(job, rows[r], s, sh, C, rank, n_ex, c, rc)) return false;
+    set_cut(s, rc);
+  }
+  return true;
+}
+
+
+// bf16 rows: the window's cut from the cluster's merged counts per 16-bit key
+// (bin = K16m - key), scanned by one warp with the dense row pass's crossing rules
+// (top-k count, then the top-p mass target over exact fixed-point weights).
+// Results in sh.sc_*[r]; sh.sc_ok[r] = 0 when the window cannot decide the cut.
+__device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin, int nb,
+                                 uint32_t K16m, float m, float c, double s_all,
+                                 const TreeJob& job, CShared& sh, int r) {
+  const int lane = threadIdx.x & 31;
+  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
+  const unsigned K = topk_on ? (unsigned)job.top_k : 0u;
+  const int Cb = (nb + 31) / 32;
+  const int b_lo = min(nb, lane * Cb), b_hi = min(nb, b_lo + Cb);
+  unsigned lc = 0;
+  unsigned long long lw = 0;
+  for (int bin = b_lo; bin < b_hi; ++bin) {
+    const unsigned long long wgt =
+        to_fixed(tempered_weight(key_value(key_from16(K16m - (uint32_t)bin)), m, c));
+    wbin[bin] = wgt;
+    lc += hist[bin];
+    lw += (unsigned long long)hist[bin] * wgt;
+  }
+  __syncwarp();
+  unsigned ic = lc;
+  unsigned long long iw = lw;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned tc = __shfl_up_sync(kFull, ic, o);
+    const unsigned long long tw = __shfl_up_sync(kFull, iw, o);
+    if (lane >= o) { ic += tc; iw += tw; }
+  }
+  const unsigned base_c = ic - lc, tot_c = __shfl_sync(kFull, ic, 31);
+  const unsigned long long base_w = iw - lw;
+  int ok = 1;
+  int b_k = nb;  // no top-k: past the last bin
+  unsigned jk = 0;
+  unsigned long long s_k = 0;
+  int bcut = 0;
+  unsigned j = 0, kept = 0;
+  unsigned long long sf = 0;
+  if (topk_on) {
+    if (tot_c < K) {
+      ok = 0;
+    } else {
+      int hitbin = INT_MAX;
+      unsigned rc = base_c;
+      for (int bin = b_lo; bin < b_hi; ++bin) {
+        if (rc + hist[bin] >= K) { hitbin = bin; break; }
+        rc += hist[bin];
+      }
+      b_k = warp_min_i(hitbin);
+      if (b_k >= nb) b_k = 0;  // cannot happen when tot_c >= K; keeps indices in range
+      const int owner = __ffs(__ballot_sync(kFull, hitbin == b_k)) - 1;
+      unsigned long long rw = base_w;
+      unsigned rc2 = base_c;
+      if (lane == owner)
+        for (int bin = b_lo; bin < min(b_k, b_hi); ++bin) {
+          rc2 += hist[bin];
+          rw += (unsigned long long)hist[bin] * wbin[bin];
+        }
+      rc2 = __shfl_sync(kFull, rc2, owner);
+      rw = __shfl_sync(kFull, rw, owner);
+      jk = K - rc2;
+      s_k = rw + (unsigned long long)jk * wbin[b_k];
+      bcut = b_k; j = jk; kept = K; sf = s_k;
+    }
+  }
+  if (ok && topp_on) {
+    const unsigned long long tau = (unsigned long long)ceil(
+        (double)job.top_p * (topk_on ? (double)s_k : s_all * 4398046511104.0));
+    int hitbin = INT_MAX;
+    unsigned long long rw = base_w;
+    for (int bin = b_lo; bin < b_hi && bin <= b_k; ++bin) {
+      const unsigned cnt = (bin == b_k) ? jk : hist[bin];
+      const unsigned long long wsum = (unsigned long long)cnt * wbin[bin];
+      if (cnt && rw + wsum >= tau) { hitbin = bin; break; }
+      rw += wsum;
+    }
+    const int b_p = warp_min_i(hitbin);
+    if (b_p == INT_MAX) {
+      ok = 0;  // the window holds too little mass
+    } else {
+      const int owner = __ffs(__ballot_sync(kFull, hitbin == b_p)) - 1;
+      unsigned rc = base_c;
+      unsigned long long rw2 = base_w;
+      if (lane == owner)
+        for (int bin = b_lo; bin < min(b_p, b_hi); ++bin) {
+          rc += hist[bin];
+          rw2 += (unsigned long long)hist[bin] * wbin[bin];
+        }
+      rc = __shfl_sync(kFull, rc, owner);
+      rw2 = __shfl_sync(kFull, rw2, owner);
+      const unsigned avail = (b_p == b_k) ? jk : hist[b_p];
+      const unsigned long long w1 = wbin[b_p];
+      unsigned jj2 = avail;
+      if (w1 > 0) {
+        const unsigned long long jj = (tau - rw2 + w1 - 1) / w1;
+        jj2 = (unsigned)(jj < 1 ? 1 : (jj > avail ? avail : jj));
+      }
+      bcut = b_p; j = jj2; kept = rc + jj2; sf = rw2 + (unsigned long long)jj2 * w1;
+    }
+  }
+  if (lane == 0) {
+    sh.sc_ok[r] = ok;
+    sh.sc_bin[r] = bcut;
+    sh.sc_j[r] = j;
+    sh.sc_kept[r] = kept;
+    sh.sc_sf[r] = sf;
+    sh.sc_ncut[r] = ok ? hist[bcut] : 0u;
+  }
+}
+
+// bf16 rows: the cut of the p row (and of the q row when with_q) of node u, from
+// per-CTA key histograms merged through distributed shared memory; the cut key's
+// ties are resolved by index from the CTAs' own candidate lists.  A histogram is
+// read by the other CTAs only between the count exchange and the tie exchange.
+__device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const void* qrow,
+                                 bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
+                                 int ub, unsigned char* smem, CShared& sh, int C, uint32_t rank,
+                                 uint32_t& n_ex, float c) {
+  const int V = job.V;
+  const int nrows = with_q ? 2 : 1;
+  spec_row_stats* st[2] = {&sp, &sq};
+  const void* const rows[2] = {prow, qrow};
+  unsigned* hist[2] = {reinterpret_cast<unsigned*>(smem),
+                       reinterpret_cast<unsigned*>(smem) + kWalkBins};
+  unsigned* merged[2] = {hist[1] + kWalkBins, hist[1] + 2 * kWalkBins};
+  unsigned long long* wbin[2] = {reinterpret_cast<unsigned long long*>(merged[1] + kWalkBins),
+                                 reinterpret_cast<unsigned long long*>(merged[1] + kWalkBins) +
+                                     kWalkBins};
+  uint64_t* const cl[2] = {reinterpret_cast<uint64_t*>(wbin[1] + kWalkBins),
+                           reinterpret_cast<uint64_t*>(wbin[1] + kWalkBins) + kCandCTA};
+  float thr[2];
+  uint32_t k16m[2];
+  int nb[2];
+  bool fits[2];
+  unsigned* hp[2] = {nullptr, nullptr};
+  for (int r = 0; r < 2; ++r) {
+    thr[r] = st[r]->m - job.delta_z;
+    k16m[r] = order_key(st[r]->m) >> 16;
+    const uint32_t k16t = order_key(thr[r]) >> 16;  // lowest key the window can hold
+    fits[r] = r < nrows && k16m[r] - k16t < (uint32_t)kWalkBins;
+    nb[r] = fits[r] ? (int)(k16m[r] - k16t) + 1 : 0;
+    if (fits[r]) hp[r] = hist[r];
+    for (int i = threadIdx.x; i < nb[r]; i += CT) hist[r][i] = 0u;
+  }
+  if (threadIdx.x == 0) { sh.ncand[0] = 0u; sh.ncand[1] = 0u; }
+  __syncthreads();
+  if (!job.exact) window_collect<uint16_t>(rows, nrows, V, ua, ub, thr, cl, hp, k16m, sh);
+  __syncthreads();
+  const unsigned own_n[2] = {min(sh.ncand[0], (unsigned)kCandCTA), min(sh.ncand[1], (unsigned)kCandCTA)};
+  // a CTA whose list overflowed finds the cut key's members by a pass over its slice
+  const bool own_over[2] = {sh.ncand[0] > (unsigned)kCandCTA, sh.ncand[1] > (unsigned)kCandCTA};
+  const uint64_t counts = (uint64_t)sh.ncand[0] | ((uint64_t)sh.ncand[1] << 32);
+  const SlotRow* sl = cluster_share(&counts, 1, sh, C, rank, n_ex);
+  if (!sl) return false;
+  bool win[2] = {false, false};
+  for (int r = 0; r < nrows; ++r) win[r] = !job.exact && fits[r];
+  // merge the key counts of every CTA (same order, integer sums: identical everywhere)
+  for (int r = 0; r < nrows; ++r) {
+    if (!win[r]) continue;
+    for (int i = threadIdx.x; i < nb[r]; i += CT) {
+      unsigned t = 0;
+      for (int q = 0; q < C; ++q) t += ld_peer_u32(peer_addr(hist[r] + i, q));
+      merged[r][i] = t;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if (warp < nrows) {
+    if (win[warp])
+      bf16_window_scan(merged[warp], wbin[warp], nb[warp], k16m[warp], st[warp]->m, c,
+                       st[warp]->s_f, job, sh, warp);
+    else if ((threadIdx.x & 31) == 0)
+      sh.sc_ok[warp] = 0;
+  }
+  if (threadIdx.x < 2) { sh.tie_cnt[threadIdx.x] = 0u; sh.tie_max[threadIdx.x] = -1; }
+  __syncthreads();
+  bool ok[2] = {false, false};
+  for (int r = 0; r < nrows; ++r) ok[r] = sh.sc_ok[r] != 0;
+  uint32_t cut32[2] = {0u, 0u};
+  if (ok[0] || ok[1]) {
+    // members of the cut key in this CTA's candidate list
+    for (int r = 0; r < nrows; ++r) {
+      if (!ok[r]) continue;
+      cut32[r] = key_from16(k16m[r] - (uint32_t)sh.sc_bin[r]);
+      if (own_over[r]) {
+        for (int u = ua + threadIdx.x; u < ub; u += CT) {
+          float z[8];
+          Elt<uint16_t>::unpack(load_raw<uint16_t>(rows[r], V, u), z);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (order_key(z[e]) == cut32[r]) {
+              atomicAdd(&sh.tie_cnt[r], 1u);
+              atomicMax(&sh.tie_max[r], u * 8 + e);
+            }
+        }
+      } else {
+        for (unsigned i = threadIdx.x; i < own_n[r]; i += CT) {
+          const uint64_t e = cl[r][i];
+          if ((uint32_t)(e >> 32) == cut32[r]) {
+            atomicAdd(&sh.tie_cnt[r], 1u);
+            atomicMax(&sh.tie_max[r], (int)(~(uint32_t)e));
+          }
+        }
+      }
+    }
+    __syncthreads();
+    uint64_t tw[2];
+    for (int r = 0; r < 2; ++r)
+      tw[r] = (uint64_t)sh.tie_cnt[r] | ((uint64_t)(uint32_t)sh.tie_max[r] << 32);
+    const SlotRow* ts = cluster_share(tw, 2, sh, C, rank, n_ex);
+    if (!ts) return false;
+    // the cut index: the largest member when the whole group is kept, else the
+    // j-th member in index order, found by the CTA whose slice holds it
+    int owner[2] = {-1, -1};
+    unsigned jr[2] = {0u, 0u};
+    int cut_idx[2] = {0, 0};
+    bool need = false;
+    for (int r = 0; r < nrows; ++r) {
+      if (!ok[r]) continue;
+      if (sh.sc_j[r] == sh.sc_ncut[r]) {
+        int mx = -1;
+        for (int q = 0; q < C; ++q) mx = max(mx, (int)(uint32_t)(ts[q][r] >> 32));
+        cut_idx[r] = mx;
+      } else {
+        unsigned before = 0;
+        for (int q = 0; q < C; ++q) {
+          const unsigned n = (unsigned)ts[q][r];
+          if (owner[r] < 0 && before + n >= sh.sc_j[r]) { owner[r] = q; jr[r] = sh.sc_j[r] - before; }
+          before += n;
+        }
+        need = true;
+      }
+    }
+    if (need) {
+      // every CTA finished reading the histograms before the tie exchange; the
+      // merged counts are no longer needed and hold the owner's member indices
+      if (threadIdx.x < 2) { sh.mem_n[threadIdx.x] = 0u; sh.tie_idx[threadIdx.x] = -1; }
+      __syncthreads();
+      for (int r = 0; r < nrows; ++r) {
+        if (owner[r] != (int)rank) continue;
+        // gather this CTA's members of the cut key (at most kWalkBins of them;
+        // more leaves the row to the exact selection)
+        if (own_over[r]) {
+          for (int u = ua + threadIdx.x; u < ub; u += CT) {
+            float z[8];
+            Elt<uint16_t>::unpack(load_raw<uint16_t>(rows[r], V, u), z);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (order_key(z[e]) == cut32[r]) {
+                const unsigned pos = atomicAdd(&sh.mem_n[r], 1u);
+                if (pos < (unsigned)kWalkBins) merged[r][pos] = (unsigned)(u * 8 + e);
+              }
+          }
+        } else {
+          for (unsigned i = threadIdx.x; i < own_n[r]; i += CT) {
+            const uint64_t e = cl[r][i];
+            if ((uint32_t)(e >> 32) == cut32[r]) {
+              const unsigned pos = atomicAdd(&sh.mem_n[r], 1u);
+              merged[r][pos] = ~(uint32_t)e;
+            }
+          }
+        }
+      }
+      __syncthreads();
+      for (int r = 0; r < nrows; ++r) {
+        if (owner[r] != (int)rank) continue;
+        const unsigned nm = sh.mem_n[r];
+        if (nm > (unsigned)kWalkBins) continue;  // tie_idx stays -1: the exact selection decides
+        for (unsigned i = threadIdx.x; i < nm; i += CT) {
+          const unsigned me = merged[r][i];
+          unsigned rk = 0;
+          for (unsigned t = 0; t < nm; ++t) rk += (merged[r][t] < me);
+          if (rk + 1 == jr[r]) sh.tie_idx[r] = (int)me;
+        }
+      }
+      __syncthreads();
+      uint64_t iw[2] = {0ull, 0ull};
+      for (int r = 0; r < 2; ++r)
+        if (owner[r] == (int)rank) iw[r] = (uint64_t)(uint32_t)sh.tie_idx[r];
+      const SlotRow* xs = cluster_share(iw, 2, sh, C, rank, n_ex);
+      if (!xs) return false;
+      for (int r = 0; r < nrows; ++r) {
+        if (!ok[r] || owner[r] < 0) continue;
+        cut_idx[r] = (int)(uint32_t)xs[owner[r]][r];
+        if (cut_idx[r] < 0) ok[r] = false;  // too many tied members: exact selection
+      }
+    }
+    for (int r = 0; r < nrows; ++r) {
+      if (!ok[r]) continue;
+      RowCut rc;
+      rc.key = cut32[r];
+      rc.idx = cut_idx[r];
+      rc.kept = sh.sc_kept[r];
+      rc.mass = sh.sc_sf[r];
+      set_cut(*st[r], rc);
+    }
+  }
+  for (int r = 0; r < nrows; ++r) {
+    if (ok[r]) continue;
+    RowCut rc;
+    if (!shared_exact_cut<uint16_t>(job, rows[r], *st[r], sh, C, rank, n_ex, c, rc)) return false;
+    set_cut(*st[r], rc);
+  }
+  return true;
+}
+
+template <typename T>
+__device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qrow, bool with_q,
+                            spec_row_stats& sp, spec_row_stats& sq, int ua, int ub,
+                            unsigned char* smem, uint32_t n_visit, CShared& sh, int C,
+                            uint32_t rank, uint32_t& n_ex, float c) {
+  if constexpr (sizeof(T) == 2) {
+    return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, c);
+  } else {
+    // candidate lists alternate between two sets from node to node (they are read
+    // by the other CTAs); then the two sort buffers
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem) + (size_t)(n_visit & 1) * 2 * kCandCTA;
+    uint64_t* sortb = reinterpret_cast<uint64_t*>(smem) + 4 * kCandCTA;
+    return cluster_cut_sorted<T>(job, prow, qrow, with_q, sp, sq, ua, ub, cand, sortb, sh, C,
+                                 rank, n_ex, c);
+  }
+}
+
+// Shared-memory bytes of the cut's buffers.
+template <typename T>
+constexpr size_t cut_smem_bytes() {
+  return sizeof(T) == 2
+             ? (size_t)kWalkBins * (4 * sizeof(unsigned) + 2 * sizeof(unsigned long long)) +
+                   2 * (size_t)kCandCTA * sizeof(uint64_t)
+             : (4 * (size_t)kCandCTA + 2 * (size_t)kSortW) * sizeof(uint64_t);
+}
+
+// ---------------------------------------------------------------------------
 // Sampling walk: one cluster of C CTAs per tree.
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -580,6 +1226,9 @@ __global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C,
   double* Z = reinterpret_cast<double*>(tsm + ((4 * N + 1 + 1) & ~1));
   float* invz = reinterpret_cast<float*>(Z + N);
   float* steps = invz + N;
+  // the top-k / top-p cut's buffers (16-byte aligned)
+  unsigned char* cut_smem = reinterpret_cast<unsigned char*>(
+      reinterpret_cast<uintptr_t>(steps + CW * max_steps + 3) & ~(uintptr_t)15);
   const double Td = (double)job.temperature;
   const float c = job.c;
   const bool lead = (rank == 0);
@@ -598,11 +1247,12 @@ __global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C,
   int32_t* out_tok = job.out_tokens + (int64_t)b * W;
   int32_t* out_path = job.out_path + (int64_t)b * W;
   uint32_t n_ex = 0;
+  uint32_t n_visit = 0;
   bool timed_out = false;
   int u = 0, n_acc = 0, final_tok = -1, owner = -1;
 
   while (status == SPEC_TREE_OK) {
-    const spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
+    spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
     if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
     const int c0 = cs[u], c1 = cs[u + 1];
     const void* prow = row_at(job.base_p, job, b, u, Elt<T>::kBytes);
@@ -611,6 +1261,15 @@ __global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C,
     if (c1 > c0) {
       sq = job.stats_q[(int64_t)b * N + u];
       if (sq.status != SPEC_TREE_OK) { status = sq.status; break; }
+    }
+    if (job.trunc) {
+      // cut the visited rows
+      if (!cluster_cut<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, cut_smem, n_visit++, sh, C,
+                          rank, n_ex, c)) {
+        timed_out = true;
+        status = SPEC_ROW_TIMEOUT;
+        break;
+      }
     }
     if (threadIdx.x == 0) {
       sh.inv_sp = (float)(1.0 / sp.s_f);
@@ -730,8 +1389,9 @@ cudaError_t launch_sampling(const TreeJob& job, cudaStream_t s) {
   const int units = (job.V + E - 1) / E;
   const int slice = (units + C - 1) / C;
   const int max_steps = max(1, ((slice + CW - 1) / CW + 31) / 32);
-  const size_t dyn = tree_smem_bytes(job.N) + (size_t)job.N * (sizeof(double) + sizeof(float)) +
-                     (size_t)CW * max_steps * sizeof(float);
+  size_t dyn = tree_smem_bytes(job.N) + (size_t)job.N * (sizeof(double) + sizeof(float)) +
+               (size_t)CW * max_steps * sizeof(float);
+  if (job.trunc) dyn += 16 + cut_smem_bytes<T>();  // 16-byte alignment + the cut's buffers
   if (dyn > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         cluster_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);

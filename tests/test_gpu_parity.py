@@ -209,7 +209,15 @@ def test_exact_select_flag_gives_identical_outputs():
     for key in ("accept_len", "tokens", "path", "status"):
         np.testing.assert_array_equal(a[key], b[key])
     np.testing.assert_array_equal(a["alpha"], b["alpha"])
-    assert b["counters"]["fallback_rows"] == b["counters"]["dense_rows"]
+    # the walk cuts the rows it visits: the p row of every node on the accepted path
+    # and the q row of those with children; the flag sends each through the exact
+    # full-row selection
+    cut_rows = 0
+    for t in range(w.B):
+        path = b["path"][t][: b["accept_len"][t] + 1]
+        has_child = set(inp["parents"][t][1:].tolist())
+        cut_rows += len(path) + sum(int(n) in has_child for n in path)
+    assert b["counters"]["fallback_rows"] == cut_rows
 
 
 def test_top1_sampling_equals_greedy_on_gpu():

@@ -38,7 +38,9 @@ METRIC = "verified draft-node logit rows/sec and achieved HBM GB/s vs GB300 peak
 UNIT = "rows/s"
 DEFAULT_WORKLOAD = "tree60_b64_v128256"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+REFERENCE_BUDGET_S = 90.0  # host seconds the reference arm's timed sample may take
 ROW_PASS_SOURCES = ["speculative_decoding_tree_spec_gb300/csrc/rows.cu",
+                    "speculative_decoding_tree_spec_gb300/csrc/select.cuh",
                     "speculative_decoding_tree_spec_gb300/csrc/common.cuh",
                     "speculative_decoding_tree_spec_gb300/csrc/internal.h"]
 
@@ -239,20 +241,26 @@ def run_reference(args):
         w = w.with_(B=args.batch)
     threads = os.cpu_count() or 1
     pool = oracle_pool(w, args.seed, min(16, w.B), "cpu")
-    time_oracle(w, pool, args.warmup, threads, args.seed)
-    wall, rows = time_oracle(w, pool, args.steps, threads, args.seed)
+    # a step is one tree verified by the oracle; the timed sample is bounded so that
+    # the run ends within a few minutes whatever --steps asks for
+    n_warm = max(1, min(args.warmup, threads))
+    wall_w, _ = time_oracle(w, pool, n_warm, threads, args.seed)
+    per_step = wall_w / n_warm
+    n_timed = min(args.steps, max(threads, int(REFERENCE_BUDGET_S / max(per_step, 1e-9))))
+    wall, rows = time_oracle(w, pool, n_timed, threads, args.seed)
     value = rows / wall
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / n_timed,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "N": w.N, "V": w.V, "logits": w.dtype,
                    "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
                    "step": "one tree verified by the CPU oracle (steps run on a host thread pool)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} tree-steps cycling over {pool['p'].shape[0]} "
-                                   f"seeded trees of {w.name}"},
+                         "sample": f"{n_timed} of the {args.steps} requested tree-steps timed "
+                                   f"(at most {REFERENCE_BUDGET_S:.0f} s of host time), cycling "
+                                   f"over {pool['p'].shape[0]} seeded trees of {w.name}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

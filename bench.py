@@ -96,6 +96,12 @@ def shard_seed(seed: int, rank: int) -> int:
     return seed + 1000003 * rank
 
 
+def whole_job_rate(world: int, units_per_step: int, steps: int, elapsed_ms_max: float) -> float:
+    """Units per second over all ranks: every rank does units_per_step per step, and the
+    job takes as long as its slowest rank."""
+    return world * units_per_step * steps / (elapsed_ms_max / 1e3)
+
+
 # ---------------------------------------------------------------------------
 # peaks, clocks, profiles
 # ---------------------------------------------------------------------------
@@ -324,7 +330,7 @@ def run_ours(args):
     row_avg_ms = sum(row_ms) / K
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     rows_per_step = w.B * w.N
-    value = world * rows_per_step * K / (elapsed_ms / 1e3)
+    value = whole_job_rate(world, rows_per_step, K, elapsed_ms)
     ms_per_step = elapsed_ms / K
 
     peaks, peak_kind = load_peaks()
@@ -353,7 +359,7 @@ def run_ours(args):
                    "l2": f"inputs {2 * w.B * w.N * w.V * (2 if w.dtype == 'bf16' else 4) / 1e9:.2f}"
                          " GB per step, larger than L2; no flush",
                    "parallelism": f"weak: {world} rank(s) x {w.B} trees"},
-        "tokens_per_s": world * tokens_per_step * K / (elapsed_ms / 1e3),
+        "tokens_per_s": whole_job_rate(world, tokens_per_step, K, elapsed_ms),
         "step_hbm_gbs": (counters["dense_bytes"] + counters["walk_bytes"]) / (ms_per_step / 1e3) / 1e9,
         "work_per_step": counters,
         "roofline": roofline,

@@ -40,7 +40,9 @@ constexpr int kSlotW = 4;      // 64-bit words one CTA can push in one exchange
 constexpr int kCandCTA = 512;  // window candidates one CTA keeps per row
 constexpr int kSortW = 2048;   // largest window (per row) the walk resolves by sorting
 constexpr int kSortPer = kSortW / CT;
-constexpr int kWalkBins = 1024;  // bf16: one bin per key in the window below the row maximum
+constexpr int kWalkBins = 1024;
+constexpr int kWalkCtasPerSm = 2;  // resident sampling-walk CTAs per SM (register budget)
+constexpr int kPreKids = 16;   // children whose accept-test inputs are prepared in parallel  // bf16: one bin per key in the window below the row maximum
 static_assert(CT == kSelThreads, "the exact selection runs on one walk CTA");
 
 __device__ __forceinline__ const void* row_at(const void* base, const TreeJob& j, int b, int n,
@@ -63,33 +65,55 @@ __device__ int load_tree(const TreeJob& job, int b, int32_t* par, int32_t* tok, 
     tok[n] = job.tokens[(int64_t)b * N + n];
     if (init_alpha && job.out_alpha) job.out_alpha[(int64_t)b * N + n] = __int_as_float(0x7fc00000);
   }
+  for (int u = threadIdx.x; u <= N; u += blockDim.x) cs[u] = 0;
   __syncthreads();
   int bad = 0;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    if (n == 0) bad |= (par[0] != -1);
-    else bad |= (par[n] < 0 || par[n] >= n || tok[n] < 0 || tok[n] >= V);
+    if (n == 0) {
+      bad |= (par[0] != -1);
+    } else {
+      bad |= (par[n] < 0 || par[n] >= n || tok[n] < 0 || tok[n] >= V);
+    }
   }
   bad = __syncthreads_or(bad);
-  if (threadIdx.x == 0) {
-    int status = bad ? SPEC_TREE_INVALID : SPEC_TREE_OK;
-    if (!bad) {
-      // depths (kept in the child array until the lists are built) and the depth limit
-      cl[0] = 0;
-      for (int n = 1; n < N; ++n) {
-        cl[n] = cl[par[n]] + 1;
-        if (cl[n] > W - 1) { status = SPEC_TREE_INVALID; break; }
-      }
+  if (!bad) {
+    // depth of every node (its ancestor chain reaches the root within W - 1 steps) and
+    // the number of children of every node
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      int x = n, d = 0;
+      while (x != 0 && d < W) { x = par[x]; ++d; }
+      bad |= (x != 0 || d > W - 1);  // deeper than max_depth
+      if (n > 0) atomicAdd(&cs[par[n] + 1], 1);
     }
-    if (status == SPEC_TREE_OK) {
-      for (int u = 0; u <= N; ++u) cs[u] = 0;
-      for (int n = 1; n < N; ++n) cs[par[n] + 1] += 1;
-      for (int u = 1; u <= N; ++u) cs[u] += cs[u - 1];
-      for (int n = 1; n < N; ++n) cl[cs[par[n]]++] = n;
-      for (int u = N; u >= 1; --u) cs[u] = cs[u - 1];
-      cs[0] = 0;
-    }
-    *s_status = status;
   }
+  bad = __syncthreads_or(bad);
+  if (!bad) {
+    // child-list offsets: inclusive scan of the counts (one warp)
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const int per = (N + 1 + 31) / 32;
+      const int lo = min(N + 1, lane * per), hi = min(N + 1, lo + per);
+      int run = 0;
+      for (int i = lo; i < hi; ++i) { run += cs[i]; cs[i] = run; }
+      int incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int base = incl - run;
+      for (int i = lo; i < hi; ++i) cs[i] += base;
+    }
+    __syncthreads();
+    // node n goes after its earlier siblings, so every list is in increasing node order
+    for (int n = threadIdx.x + 1; n < N; n += blockDim.x) {
+      const int u = par[n];
+      int before = 0;
+      for (int m = u + 1; m < n; ++m) before += (par[m] == u);
+      cl[cs[u] + before] = n;
+    }
+  }
+  if (threadIdx.x == 0) *s_status = bad ? SPEC_TREE_INVALID : SPEC_TREE_OK;
   __syncthreads();
   return *s_status;
 }
@@ -283,14 +307,14 @@ __device__ __forceinline__ void residual_chain(float (&p)[E], const float (&q)[E
 // their sum in element order.  Both inverse-CDF phases call this, so a unit
 // always yields the same values and sum.
 template <typename T>
-__device__ __forceinline__ float dist_unit(const void* prow, const void* qrow, int V, int u,
-                                           const RowF& fp, const RowF& fq, int j,
-                                           const float* invz, float (&val)[Elt<T>::kPerUnit]) {
+__device__ __forceinline__ float dist_from_raw(uint4 rp, uint4 rq, int u, const RowF& fp,
+                                               const RowF& fq, int j, const float* invz,
+                                               float (&val)[Elt<T>::kPerUnit]) {
   constexpr int E = Elt<T>::kPerUnit;
-  unit_probs<T>(load_raw<T>(prow, V, u), u * E, fp, val);
+  unit_probs<T>(rp, u * E, fp, val);
   if (j > 0) {
     float q[E];
-    unit_probs<T>(load_raw<T>(qrow, V, u), u * E, fq, q);
+    unit_probs<T>(rq, u * E, fq, q);
     residual_chain<E>(val, q, j, invz);
   }
   float s = 0.f;
@@ -299,12 +323,16 @@ __device__ __forceinline__ float dist_unit(const void* prow, const void* qrow, i
   return s;
 }
 
+// Is the token x with order key k inside the kept set of a filtered row?
+__device__ __forceinline__ bool kept_key(uint32_t k, int x, const spec_row_stats& st) {
+  return k > st.cut_key || (k == st.cut_key && x <= st.cut_idx);
+}
+
 // Filtered probability of one token in fp64 (for the acceptance test).
 template <typename T>
 __device__ double prob64(const void* row, int x, const spec_row_stats& st, double T_) {
   const float z = Elt<T>::at(row, x);
-  const uint32_t k = order_key(z);
-  if (!(k > st.cut_key || (k == st.cut_key && x <= st.cut_idx))) return 0.0;
+  if (!kept_key(order_key(z), x, st)) return 0.0;
   return exp(((double)z - (double)st.m) / T_) / st.s_f;
 }
 
@@ -338,9 +366,6 @@ __device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
   return v;
-}
-__device__ __forceinline__ void fence_cluster() {
-  asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
 }
 __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_addr)
@@ -390,6 +415,12 @@ struct CShared {
   unsigned sc_j[2], sc_kept[2], sc_ncut[2];
   unsigned long long sc_sf[2];
   unsigned tie_cnt[2], mem_n[2];
+  // accept-test inputs of the first kPreKids children of the current node: the
+  // unnormalised fp64 weights of the drafted token under p and q, its order keys,
+  // and its accept uniform
+  double kid_e[2][kPreKids];
+  uint32_t kid_k[2][kPreKids];
+  double kid_u[kPreKids];
   int tie_max[2], tie_idx[2];
   SelShared sel;
 };
@@ -410,12 +441,19 @@ __device__ const SlotRow* cluster_share(const uint64_t* v, int nv, CShared& sh, 
   const int set = n_ex & 1;
   const uint32_t parity = (n_ex >> 1) & 1u;
   ++n_ex;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    fence_cluster();
-    for (int c = 0; c < C; ++c) {
-      for (int w = 0; w < nv; ++w) st_peer_u64(peer_addr(&sh.slot[set][rank][w], c), v[w]);
-      arrive_peer(peer_addr(&sh.xbar[set], c));
+  __syncthreads();  // the CTA's earlier writes happen before the releasing arrives below
+  if (threadIdx.x < 32) {
+    // thread t pushes thread 0's words to CTA t (all targets at once)
+    uint64_t w[kSlotW];
+#pragma unroll
+    for (int k = 0; k < kSlotW; ++k)
+      w[k] = __shfl_sync(kFull, (threadIdx.x == 0 && k < nv) ? v[k] : 0ull, 0);
+    if ((int)threadIdx.x < C) {
+      const uint32_t t = threadIdx.x;
+#pragma unroll
+      for (int k = 0; k < kSlotW; ++k)
+        if (k < nv) st_peer_u64(peer_addr(&sh.slot[set][rank][k], t), w[k]);
+      arrive_peer(peer_addr(&sh.xbar[set], t));
     }
   }
   const bool ok = __syncthreads_and(mbar_wait_cluster(&sh.xbar[set], parity, kExchangeLimitNs));
@@ -528,13 +566,28 @@ __device__ int cluster_inverse_cdf(const void* prow, const void* qrow, int V, in
   float* st = steps + warp * max_steps;
   FF wt;
   int ns = 0;
-  for (int base_u = lo; base_u < hi; base_u += 32, ++ns) {
-    const int u = base_u + lane;
-    float val[E];
-    const float s = (u < hi) ? dist_unit<T>(prow, qrow, V, u, fp, fq, j, invz, val) : 0.f;
-    const float it = warp_sum_f(s);
-    if (lane == 0) st[ns] = it;
-    wt.add(it);
+  constexpr int kSteps = 4;  // 32-unit steps whose loads are issued before any is used
+  for (int base_u = lo; base_u < hi; base_u += 32 * kSteps) {
+    uint4 rp[kSteps], rq[kSteps];
+#pragma unroll
+    for (int h = 0; h < kSteps; ++h) {
+      const int u = base_u + 32 * h + lane;
+      if (u < hi) {
+        rp[h] = load_raw<T>(prow, V, u);
+        if (j > 0) rq[h] = load_raw<T>(qrow, V, u);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kSteps; ++h) {
+      if (base_u + 32 * h >= hi) break;
+      const int u = base_u + 32 * h + lane;
+      float val[E];
+      const float s = (u < hi) ? dist_from_raw<T>(rp[h], rq[h], u, fp, fq, j, invz, val) : 0.f;
+      const float it = warp_sum_f(s);
+      if (lane == 0) st[ns] = it;
+      wt.add(it);
+      ++ns;
+    }
   }
   if (lane == 0) sh.wtot[warp] = wt.value();
   __syncthreads();
@@ -583,7 +636,12 @@ __device__ int cluster_inverse_cdf(const void* prow, const void* qrow, int V, in
     if (s_hit >= 0) {
       const int u = lo + 32 * s_hit + lane;
       float val[E];
-      const float s = (u < hi) ? dist_unit<T>(prow, qrow, V, u, fp, fq, j, invz, val) : 0.f;
+      float s = 0.f;
+      if (u < hi) {
+        const uint4 rp = load_raw<T>(prow, V, u);
+        const uint4 rq = (j > 0) ? load_raw<T>(qrow, V, u) : rp;
+        s = dist_from_raw<T>(rp, rq, u, fp, fq, j, invz, val);
+      }
       float incl = s;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -648,16 +706,23 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
                                unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
                                CShared& sh) {
   constexpr int E = Elt<T>::kPerUnit;
-  for (int u = ua + threadIdx.x; u < ub; u += CT) {
-    uint4 raw[2];
+  constexpr int kBatch = 2;  // units of each row loaded before any is used
+  for (int u0 = ua + threadIdx.x; u0 < ub; u0 += CT * kBatch) {
+  uint4 rb[2][kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
 #pragma unroll
     for (int r = 0; r < 2; ++r)
-      if (r < nrows) raw[r] = load_raw<T>(rows[r], V, u);
+      if (r < nrows && u0 + k * CT < ub) rb[r][k] = load_raw<T>(rows[r], V, u0 + k * CT);
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    const int u = u0 + k * CT;
+    if (u >= ub) break;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;
       float z[E];
-      Elt<T>::unpack(raw[r], z);
+      Elt<T>::unpack(rb[r][k], z);
       float mx = z[0];
 #pragma unroll
       for (int e = 1; e < E; ++e) mx = fmaxf(mx, z[e]);
@@ -677,6 +742,7 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
         }
       }
     }
+  }
   }
 }
 
@@ -1213,7 +1279,7 @@ constexpr size_t cut_smem_bytes() {
 // Sampling walk: one cluster of C CTAs per tree.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C, int max_steps) {
+__global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJob job, int C, int max_steps) {
   __shared__ CShared sh;
   // parents [N], tokens [N], child offsets [N+1], children [N]; then Z [N] (fp64),
   // 1/Z [N] and the per-warp step totals [CW][max_steps]
@@ -1262,6 +1328,17 @@ __global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C,
       sq = job.stats_q[(int64_t)b * N + u];
       if (sq.status != SPEC_TREE_OK) { status = sq.status; break; }
     }
+    // the first children's accept-test inputs, one lane per (child, row) of warp 0;
+    // they do not depend on the cut and overlap the rest of the block's work
+    const int n_pre = min(c1 - c0, kPreKids);
+    if (threadIdx.x < 2 * n_pre) {
+      const int i = (int)threadIdx.x % n_pre, r = (int)threadIdx.x / n_pre;
+      const int ch = cl[c0 + i];
+      const float z = Elt<T>::at(r ? qrow : prow, tok[ch]);
+      sh.kid_e[r][i] = exp(((double)z - (double)(r ? sq.m : sp.m)) / Td);
+      sh.kid_k[r][i] = order_key(z);
+      if (r == 0) sh.kid_u[i] = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
+    }
     if (job.trunc) {
       // cut the visited rows
       if (!cluster_cut<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, cut_smem, n_visit++, sh, C,
@@ -1282,14 +1359,22 @@ __global__ void __launch_bounds__(CT, 3) cluster_walk_kernel(TreeJob job, int C,
       const int ch = cl[i];
       if (threadIdx.x == 0) {
         const int x = tok[ch];
-        double P = prob64<T>(prow, x, sp, Td);
-        const double Q = prob64<T>(qrow, x, sq, Td);
+        double P, Q, uu;
+        if (i - c0 < kPreKids) {
+          const int k = i - c0;
+          P = kept_key(sh.kid_k[0][k], x, sp) ? sh.kid_e[0][k] / sp.s_f : 0.0;
+          Q = kept_key(sh.kid_k[1][k], x, sq) ? sh.kid_e[1][k] / sq.s_f : 0.0;
+          uu = sh.kid_u[k];
+        } else {
+          P = prob64<T>(prow, x, sp, Td);
+          Q = prob64<T>(qrow, x, sq, Td);
+          uu = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
+        }
         for (int r = 0; r < j; ++r)
           if (Z[r] > 0.0) P = fmax(0.0, P - Q) / Z[r];
         const double alpha = (Q > 0.0) ? fmin(1.0, P / Q) : (P > 0.0 ? 1.0 : 0.0);
-        const uint4 w = philox_words(job.seed, job.offset, b, ch);
         if (lead && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = (float)alpha;
-        sh.accept = (unit_uniform(w.x) <= alpha);
+        sh.accept = (uu <= alpha);
       }
       __syncthreads();
       const int acc = sh.accept;
@@ -1373,11 +1458,12 @@ int floor_pow2(int x) {
   return p;
 }
 
-// CTAs per tree: enough to give about four CTAs per SM over all trees, at most
-// kMaxC, and at least two 256-thread rounds of units per CTA.
+// CTAs per tree: as many as keep every tree's cluster resident at once (the SMs
+// hold kWalkCtasPerSm CTAs each), at most kMaxC, and at least two 256-thread
+// rounds of units per CTA.
 int cluster_size(int B, int V, int E) {
   const int units = (V + E - 1) / E;
-  int C = floor_pow2(max(1, 4 * device_sm_count() / max(B, 1)));
+  int C = floor_pow2(max(1, kWalkCtasPerSm * device_sm_count() / max(B, 1)));
   C = min(C, floor_pow2(max(1, units / (2 * CT))));
   return max(1, min(C, kMaxC));
 }

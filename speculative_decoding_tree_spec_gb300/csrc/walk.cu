@@ -731,9 +731,12 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
         for (int e = 0; e < E; ++e) {
           if (z[e] >= thr[r]) {
             const uint32_t k = order_key(z[e]);
-            const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
-            if (pos < (unsigned)kCandCTA)
-              cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
+            // once the list is full only the overflow matters: stop counting
+            if (*((volatile unsigned*)&sh.ncand[r]) <= (unsigned)kCandCTA) {
+              const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
+              if (pos < (unsigned)kCandCTA)
+                cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
+            }
             if (hist[r]) {
               const uint32_t bin = k16m[r] - (k >> 16);
               if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
@@ -1081,8 +1084,14 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   for (int r = 0; r < 2; ++r) {
     thr[r] = st[r]->m - job.delta_z;
     k16m[r] = order_key(st[r]->m) >> 16;
-    const uint32_t k16t = order_key(thr[r]) >> 16;  // lowest key the window can hold
-    fits[r] = r < nrows && k16m[r] - k16t < (uint32_t)kWalkBins;
+    uint32_t k16t = order_key(thr[r]) >> 16;  // lowest key the window can hold
+    if (k16m[r] - k16t >= (uint32_t)kWalkBins) {
+      // clip the window to the kWalkBins keys below the maximum; the scan checks that
+      // it still holds the cut (else the exact selection decides)
+      k16t = k16m[r] - (uint32_t)(kWalkBins - 1);
+      thr[r] = key_value(key_from16(k16t));
+    }
+    fits[r] = r < nrows;
     nb[r] = fits[r] ? (int)(k16m[r] - k16t) + 1 : 0;
     if (fits[r]) hp[r] = hist[r];
     for (int i = threadIdx.x; i < nb[r]; i += CT) hist[r][i] = 0u;

@@ -288,7 +288,7 @@ def run_ours(args):
     if args.batch:
         w = w.with_(B=args.batch)
     if w.logits == "lmhead":
-        raise SystemExit("the fused LM-head workload is not wired into bench.py yet")
+        return run_ours_lmhead(args, w, world, rank, local, dev)
     seed = shard_seed(args.seed, rank)
     inp = wl.build_inputs(w, seed=seed, device=dev)
     tok = torch.as_tensor(inp["tokens"], device=dev)
@@ -375,6 +375,121 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_ours_lmhead(args, w, world, rank, local, dev):
+    """The fused LM-head workload: every step computes the target logits of all B*N
+    nodes from their features on the tensor cores (with the row statistics), the draft
+    rows' statistics, and the walk.  The roofline is the LM-head GEMM's FLOP rate."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    seed = shard_seed(args.seed, rank)
+    inp = wl.build_lmhead_inputs(w, seed, device=dev)
+    tok = torch.as_tensor(inp["tokens"], device=dev)
+    par = torch.as_tensor(inp["parents"], device=dev)
+    args_ = (inp["features"], inp["weight"], inp["q"], tok, par, inp["max_depth"], w.temperature,
+             w.top_k, w.top_p)
+    first = binding.verify_tree_fused_lmhead(*args_, seed=seed, want_counters=True)
+    out = {k: v for k, v in first.items() if torch.is_tensor(v)}
+    ws = torch.empty(max(256, int(binding.lib().spec_fused_lmhead_workspace_size(w.B, w.N, w.V))),
+                     dtype=torch.uint8, device=dev)
+    counters = first["counters"]
+
+    def call(phases):
+        binding.verify_tree_fused_lmhead(*args_, seed=seed, out=out, workspace=ws, phases=phases)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call(binding.SPEC_PHASE_ALL_FUSED)
+    acc = out["accept_len"].cpu().numpy()
+    tokens_per_step = int((acc + 1).sum())
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.wait_first()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gs = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ge = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(K):
+        call(binding.SPEC_PHASE_PREPARE)
+        gs[k].record(stream)
+        call(binding.SPEC_PHASE_LMHEAD)
+        ge[k].record(stream)
+        call(binding.SPEC_PHASE_ROWS | binding.SPEC_PHASE_WALK)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    clocks.stop()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    gemm_ms = sum(gs[k].elapsed_time(ge[k]) for k in range(K)) / K
+    d = inp["features"].shape[1]
+    flops = 2.0 * w.B * w.N * w.V * d
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops / (gemm_ms / 1e3) / 1e12
+    result = {
+        "metric": METRIC, "value": whole_job_rate(world, w.B * w.N, K, elapsed_ms), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": elapsed_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "V": w.V, "d": d, "logits": "bf16",
+                   "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
+                   "tree": f"{w.tree}, depth {inp['max_depth']}, branching <= {w.max_branch}",
+                   "l2": f"weight {w.V * d * 2 / 1e9:.2f} GB + logits written "
+                         f"{w.B * w.N * w.V * 2 / 1e9:.2f} GB per step, larger than L2; no flush",
+                   "parallelism": f"weak: {world} rank(s) x {w.B} trees"},
+        "tokens_per_s": whole_job_rate(world, tokens_per_step, K, elapsed_ms),
+        "work_per_step": counters,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "lmhead_kernel (tcgen05 GEMM + row statistics) + combine",
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                     "algorithmic_flops_per_launch": flops, "avg_launch_ms": gemm_ms},
+        "gpu_launches": 4 * K if w.temperature > 0 else 3 * K,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    if not args.no_e2e:
+        host = {"features": inp["features"].cpu().pin_memory(),
+                "q": inp["q"].cpu().pin_memory(),
+                "tokens": torch.as_tensor(inp["tokens"]).pin_memory(),
+                "parents": torch.as_tensor(inp["parents"]).pin_memory()}
+        dbuf = {"features": torch.empty_like(inp["features"]), "q": torch.empty_like(inp["q"]),
+                "tokens": torch.empty_like(tok), "parents": torch.empty_like(par)}
+        outs = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory()
+                for k in ("accept_len", "tokens", "path")}
+
+        def step():
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            binding.verify_tree_fused_lmhead(dbuf["features"], inp["weight"], dbuf["q"],
+                                             dbuf["tokens"], dbuf["parents"], inp["max_depth"],
+                                             w.temperature, w.top_k, w.top_p, seed=seed, out=out,
+                                             workspace=ws)
+            for k, v in outs.items():
+                v.copy_(out[k], non_blocking=True)
+
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+        result["e2e"] = {"value": world * w.B * w.N / (ms / 1e3), "unit": UNIT,
+                         "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                         "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in outs.values()),
+                         "ms_per_step": ms, "steps": args.e2e_steps}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
 
 
 def run_e2e(args, w, inp, dev, stream):

@@ -229,6 +229,63 @@ int spec_verify_tree_phases(uint32_t phases, const void* logits_p, const void* l
                             spec_verify_counters* out_counters, void* workspace,
                             size_t workspace_bytes, spec_stream_t stream);
 
+/* Bytes of device workspace spec_verify_tree_fused_lmhead needs for B trees of N
+ * nodes over a vocabulary of V.  Returns 0 for invalid sizes. */
+size_t spec_fused_lmhead_workspace_size(int32_t B, int32_t N, int32_t V);
+
+/*
+ * Verify with the target logits computed here: p = F W^T, the LM head applied to the
+ * feature vector of every tree node (EAGLE obtains the target's next-token
+ * distribution of each node from its features this way: "EAGLE close reading",
+ * edgeai1.github.io, section 3), on the tensor cores, with the statistics the verify
+ * step needs taken from the product before it leaves the chip; then the verify step
+ * of spec_verify_tree.
+ *
+ * features [B*N, d] bf16, row-major (row b*N + n is node n of tree b); lm_head_w
+ *   [V, d] bf16, row-major; d a multiple of 8; both 16-byte aligned.
+ * logits_q [B, N, V] bf16 draft logits (may be NULL when temperature == 0).
+ * out_logits_p [B, N, V] bf16 (device, caller-owned): receives p, rounded to bf16
+ *   (the verify step uses these rounded logits).
+ * p and q share row_pitch (elements, >= V, row_pitch * 2 a multiple of 16 bytes);
+ *   tree b starts at row b * N (batch stride N * row_pitch).
+ * All other arguments and outputs as spec_verify_tree; workspace of at least
+ * spec_fused_lmhead_workspace_size() bytes, 256-byte aligned.  A device-side wait
+ * that gives up marks every tree SPEC_ROW_TIMEOUT.
+ * Errors: as spec_verify_tree; SPEC_ERR_MISALIGNED also for d not a multiple of 8.
+ */
+int spec_verify_tree_fused_lmhead(const void* features, const void* lm_head_w, int32_t d,
+                                  const void* logits_q, int32_t B, int32_t N, int32_t V,
+                                  int64_t row_pitch, const int32_t* draft_tokens,
+                                  const int32_t* parent_idx, int32_t max_depth,
+                                  spec_sampling_params params, uint64_t rng_seed,
+                                  uint64_t rng_offset, void* out_logits_p,
+                                  int32_t* out_accept_len, int32_t* out_tokens,
+                                  int32_t* out_accepted_path, float* out_alpha,
+                                  int32_t* out_status, spec_verify_counters* out_counters,
+                                  void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Phase of the fused call: the tensor-core LM head and the target rows' statistics
+ * (SPEC_PHASE_ROWS then covers the draft rows only). */
+#define SPEC_PHASE_LMHEAD 8u
+#define SPEC_PHASE_ALL_FUSED 15u
+
+/*
+ * spec_verify_tree_fused_lmhead split into its phases, launched in the order
+ * prepare -> lmhead -> rows -> walk for the bits set in `phases` (a subset of
+ * SPEC_PHASE_ALL_FUSED); calling them one after another on one stream with identical
+ * arguments and the same workspace equals one spec_verify_tree_fused_lmhead call.
+ * Errors as spec_verify_tree_fused_lmhead; an unknown bit or phases == 0 is
+ * SPEC_ERR_INVALID_ARG.
+ */
+int spec_verify_tree_fused_lmhead_phases(
+    uint32_t phases, const void* features, const void* lm_head_w, int32_t d,
+    const void* logits_q, int32_t B, int32_t N, int32_t V, int64_t row_pitch,
+    const int32_t* draft_tokens, const int32_t* parent_idx, int32_t max_depth,
+    spec_sampling_params params, uint64_t rng_seed, uint64_t rng_offset, void* out_logits_p,
+    int32_t* out_accept_len, int32_t* out_tokens, int32_t* out_accepted_path, float* out_alpha,
+    int32_t* out_status, spec_verify_counters* out_counters, void* workspace,
+    size_t workspace_bytes, spec_stream_t stream);
+
 /*
  * The dense row pass alone: filter R rows (row r at logits + r * row_pitch
  * elements) with `params` and write one spec_row_stats per row to out_stats

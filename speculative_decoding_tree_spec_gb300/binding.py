@@ -30,6 +30,8 @@ SPEC_PHASE_PREPARE = 1
 SPEC_PHASE_ROWS = 2
 SPEC_PHASE_WALK = 4
 SPEC_PHASE_ALL = 7
+SPEC_PHASE_LMHEAD = 8
+SPEC_PHASE_ALL_FUSED = 15
 SPEC_MAX_NODES = 4096
 SPEC_MAX_VOCAB = 1 << 21
 SPEC_STATIC_WORKSPACE_BYTES = 1 << 20
@@ -84,6 +86,15 @@ def lib():
             L.spec_verify_tree_phases.restype = ctypes.c_int
             L.spec_verify_tree_noalloc.argtypes = L.spec_verify_tree.argtypes[:20] + [P]
             L.spec_verify_tree_noalloc.restype = ctypes.c_int
+            L.spec_fused_lmhead_workspace_size.argtypes = [i32, i32, i32]
+            L.spec_fused_lmhead_workspace_size.restype = ctypes.c_size_t
+            L.spec_verify_tree_fused_lmhead.argtypes = [P, P, i32, P, i32, i32, i32, i64, P, P,
+                                                        i32, SamplingParams, u64, u64, P, P, P,
+                                                        P, P, P, P, P, ctypes.c_size_t, P]
+            L.spec_verify_tree_fused_lmhead.restype = ctypes.c_int
+            L.spec_verify_tree_fused_lmhead_phases.argtypes = (
+                [ctypes.c_uint32] + L.spec_verify_tree_fused_lmhead.argtypes)
+            L.spec_verify_tree_fused_lmhead_phases.restype = ctypes.c_int
             L.spec_filter_rows.argtypes = [P, ctypes.c_int, i32, i32, i64, SamplingParams, P, P]
             L.spec_filter_rows.restype = ctypes.c_int
             L.spec_philox_words.argtypes = [u64, u64, P, P, i32, P, P]
@@ -219,6 +230,65 @@ def verify_tree_noalloc(p: torch.Tensor, q, draft_tokens: torch.Tensor, parent_i
         _stream_ptr(stream))
     if rc != 0:
         raise SpecError(rc, "spec_verify_tree_noalloc")
+    return out
+
+
+def verify_tree_fused_lmhead(features: torch.Tensor, weight: torch.Tensor, q,
+                             draft_tokens: torch.Tensor, parent_idx: torch.Tensor, max_depth: int,
+                             temperature: float, top_k: int = 0, top_p: float = 1.0,
+                             seed: int = 0, offset: int = 0, flags: int = 0, *,
+                             want_alpha: bool = True, want_counters: bool = False,
+                             out=None, workspace=None, stream=None,
+                             phases: int = SPEC_PHASE_ALL_FUSED):
+    """spec_verify_tree_fused_lmhead on device tensors: features [B*N, d] and weight
+    [V, d] bf16, q [B, N, V] bf16 (or None at temperature 0).  Returns the dict of
+    verify_tree plus "p": the bf16 target logits [B, N, V] the call computed."""
+    B, N = draft_tokens.shape
+    V, d = weight.shape
+    dev = weight.device
+    if features.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("features and weight must be bfloat16")
+    if tuple(features.shape) != (B * N, d) or not features.is_contiguous() or \
+            not weight.is_contiguous():
+        raise ValueError("features must be contiguous [B*N, d] and weight contiguous [V, d]")
+    if draft_tokens.dtype != torch.int32 or parent_idx.dtype != torch.int32:
+        raise TypeError("draft_tokens and parent_idx must be int32")
+    W = max_depth + 1
+    if out is None:
+        out = {
+            "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+            "tokens": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "path": torch.empty((B, W), dtype=torch.int32, device=dev),
+            "status": torch.empty(B, dtype=torch.int32, device=dev),
+            # rows padded to a 16-byte aligned pitch
+            "p": torch.empty((B, N, (V + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[..., :V],
+        }
+        if want_alpha:
+            out["alpha"] = torch.empty((B, N), dtype=torch.float32, device=dev)
+    pitch = out["p"].stride(1)
+    if q is not None:
+        if q.dtype != torch.bfloat16 or tuple(q.shape) != (B, N, V) or q.stride(1) != pitch or \
+                q.stride(0) != N * pitch or q.stride(2) != 1:
+            raise ValueError("q must be bf16 [B, N, V] with the row pitch of the p output")
+    ws_bytes = int(lib().spec_fused_lmhead_workspace_size(B, N, V))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    counters = torch.zeros(8, dtype=torch.int64, device=dev) if want_counters else None
+    rc = lib().spec_verify_tree_fused_lmhead_phases(
+        int(phases), features.data_ptr(), weight.data_ptr(), d, None if q is None else q.data_ptr(), B, N, V,
+        pitch, draft_tokens.data_ptr(), parent_idx.data_ptr(), int(max_depth),
+        params(temperature, top_k, top_p, flags), int(seed) & (2**64 - 1),
+        int(offset) & (2**64 - 1), out["p"].data_ptr(), out["accept_len"].data_ptr(),
+        out["tokens"].data_ptr(), out["path"].data_ptr(),
+        out["alpha"].data_ptr() if "alpha" in out else None, out["status"].data_ptr(),
+        None if counters is None else counters.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_verify_tree_fused_lmhead")
+    if counters is not None:
+        c = counters.cpu().numpy().view("uint64")
+        out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
+                                    "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))
     return out
 
 

@@ -2,6 +2,7 @@
 // carving and the launches of one verify call on the caller's stream: (prepare)
 // zero the work counters when they are requested, (rows) the dense row pass,
 // (walk) the per-tree accept walk.
+#include <climits>
 #include <cmath>
 
 #include "internal.h"
@@ -185,6 +186,153 @@ extern "C" int spec_verify_tree(const void* logits_p, const void* logits_q, spec
                                  rng_seed, rng_offset, out_accept_len, out_tokens,
                                  out_accepted_path, out_alpha, out_status, out_counters,
                                  workspace, workspace_bytes, stream);
+}
+
+namespace {
+// Workspace of the fused call: the verify workspace, then the LM head's tile
+// statistics and its error flag (256-byte aligned sections).
+struct FusedLayout {
+  WsLayout base;
+  size_t part, err, total;
+};
+FusedLayout fused_layout(int32_t B, int32_t N, int32_t V) {
+  FusedLayout L{};
+  L.base = ws_layout(B, N);
+  L.part = L.base.total;
+  L.err = align_up(L.part + lmhead_part_bytes(B * N, V), 256);
+  L.total = align_up(L.err + sizeof(int), 256);
+  return L;
+}
+}  // namespace
+
+extern "C" size_t spec_fused_lmhead_workspace_size(int32_t B, int32_t N, int32_t V) {
+  if (B < 1 || N < 1 || V < 1 || N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB) return 0;
+  if ((int64_t)B * N > (int64_t)INT32_MAX / 2) return 0;
+  return fused_layout(B, N, V).total;
+}
+
+extern "C" int spec_verify_tree_fused_lmhead_phases(
+    uint32_t phases, const void* features, const void* lm_head_w, int32_t d, const void* logits_q, int32_t B,
+    int32_t N, int32_t V, int64_t row_pitch, const int32_t* draft_tokens,
+    const int32_t* parent_idx, int32_t max_depth, spec_sampling_params params,
+    uint64_t rng_seed, uint64_t rng_offset, void* out_logits_p, int32_t* out_accept_len,
+    int32_t* out_tokens, int32_t* out_accepted_path, float* out_alpha, int32_t* out_status,
+    spec_verify_counters* out_counters, void* workspace, size_t workspace_bytes,
+    spec_stream_t stream) {
+  if (phases == 0 || (phases & ~SPEC_PHASE_ALL_FUSED)) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || N < 1 || V < 1 || max_depth < 0 || d < 1) return SPEC_ERR_INVALID_ARG;
+  if (N > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || max_depth >= SPEC_MAX_NODES)
+    return SPEC_ERR_TOO_LARGE;
+  if ((int64_t)B * N > (int64_t)INT32_MAX / 2) return SPEC_ERR_TOO_LARGE;
+  int rc = check_params(params);
+  if (rc != SPEC_OK) return rc;
+  const bool greedy = params.temperature == 0.0f;
+  if (!features || !lm_head_w || (!greedy && !logits_q) || !draft_tokens || !parent_idx ||
+      !out_logits_p || !out_accept_len || !out_tokens || !out_accepted_path || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  // the tensor maps need 16-byte aligned bases and rows (d a multiple of 8)
+  if (!aligned16(features) || !aligned16(lm_head_w) || d % 8 != 0) return SPEC_ERR_MISALIGNED;
+  const int64_t batch_stride = (int64_t)N * row_pitch;
+  rc = check_layout(out_logits_p, SPEC_BF16, row_pitch, batch_stride, V);
+  if (rc != SPEC_OK) return rc;
+  if (!greedy) {
+    rc = check_layout(logits_q, SPEC_BF16, row_pitch, batch_stride, V);
+    if (rc != SPEC_OK) return rc;
+  }
+  if (B == 0) return SPEC_OK;
+  const FusedLayout L = fused_layout(B, N, V);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  spec_row_stats* stats_p = reinterpret_cast<spec_row_stats*>(ws + L.base.stats_p);
+  spec_row_stats* stats_q = reinterpret_cast<spec_row_stats*>(ws + L.base.stats_q);
+  unsigned long long* counters = reinterpret_cast<unsigned long long*>(ws + L.base.counters);
+  int* err = reinterpret_cast<int*>(ws + L.err);
+  unsigned long long* cnt = out_counters ? counters : nullptr;
+
+  if (phases & SPEC_PHASE_PREPARE) {
+    if (out_counters &&
+        cudaMemsetAsync(counters, 0, sizeof(spec_verify_counters), s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  // target rows: logits and their statistics from the tensor-core GEMM
+  if ((phases & SPEC_PHASE_LMHEAD) &&
+      launch_lmhead(features, lm_head_w, B * N, V, d, params.temperature, out_logits_p,
+                    row_pitch, ws + L.part, err, stats_p, cnt, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  // draft rows of nodes with children: the dense row pass
+  if (!greedy && (phases & SPEC_PHASE_ROWS)) {
+    RowJob rj = make_row_job(SPEC_BF16, V, params);
+    rj.base_p = out_logits_p;
+    rj.base_q = logits_q;
+    rj.row_pitch = row_pitch;
+    rj.batch_stride = batch_stride;
+    rj.N = N;
+    rj.B = B;
+    rj.mode = kRowsTree;
+    rj.with_q = 1;
+    rj.first_row = B * N;
+    rj.top_k = 0;
+    rj.top_p = 1.0f;
+    rj.parents = parent_idx;
+    rj.stats_p = stats_p;
+    rj.stats_q = stats_q;
+    rj.counters = cnt;
+    if (launch_row_pass(rj, SPEC_BF16, B * N, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  TreeJob tj{};
+  tj.base_p = out_logits_p;
+  tj.base_q = logits_q;
+  tj.row_pitch = row_pitch;
+  tj.batch_stride = batch_stride;
+  tj.V = V;
+  tj.N = N;
+  tj.B = B;
+  tj.W = max_depth + 1;
+  tj.tokens = draft_tokens;
+  tj.parents = parent_idx;
+  tj.stats_p = stats_p;
+  tj.stats_q = stats_q;
+  tj.temperature = params.temperature;
+  tj.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)params.temperature);
+  tj.top_k = (params.top_k > 0 && params.top_k < V) ? params.top_k : 0;
+  tj.top_p = params.top_p >= 1.0f ? 1.0f : params.top_p;
+  tj.trunc = (!greedy && (tj.top_k > 0 || tj.top_p < 1.0f)) ? 1 : 0;
+  tj.delta_z = kWindowNats * params.temperature;
+  tj.exact = (params.flags & SPEC_FLAG_EXACT_SELECT) ? 1 : 0;
+  tj.seed = rng_seed;
+  tj.offset = rng_offset;
+  tj.out_accept_len = out_accept_len;
+  tj.out_tokens = out_tokens;
+  tj.out_path = out_accepted_path;
+  tj.out_alpha = out_alpha;
+  tj.out_status = out_status;
+  tj.counters = cnt;
+  if (phases & SPEC_PHASE_WALK) {
+    if (launch_tree_walk(tj, SPEC_BF16, greedy, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (out_counters && cudaMemcpyAsync(out_counters, counters, sizeof(spec_verify_counters),
+                                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_verify_tree_fused_lmhead(
+    const void* features, const void* lm_head_w, int32_t d, const void* logits_q, int32_t B,
+    int32_t N, int32_t V, int64_t row_pitch, const int32_t* draft_tokens,
+    const int32_t* parent_idx, int32_t max_depth, spec_sampling_params params,
+    uint64_t rng_seed, uint64_t rng_offset, void* out_logits_p, int32_t* out_accept_len,
+    int32_t* out_tokens, int32_t* out_accepted_path, float* out_alpha, int32_t* out_status,
+    spec_verify_counters* out_counters, void* workspace, size_t workspace_bytes,
+    spec_stream_t stream) {
+  return spec_verify_tree_fused_lmhead_phases(
+      SPEC_PHASE_ALL_FUSED, features, lm_head_w, d, logits_q, B, N, V, row_pitch, draft_tokens,
+      parent_idx, max_depth, params, rng_seed, rng_offset, out_logits_p, out_accept_len,
+      out_tokens, out_accepted_path, out_alpha, out_status, out_counters, workspace,
+      workspace_bytes, stream);
 }
 
 extern "C" int spec_filter_rows(const void* logits, spec_dtype dtype, int32_t R, int32_t V,

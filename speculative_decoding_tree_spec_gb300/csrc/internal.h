@@ -61,6 +61,7 @@ struct RowJob {
   int32_t V, N, B, R;
   int32_t mode;
   int32_t with_q;
+  int32_t first_row;       // first virtual row of the launch (kRowsTree: B*N = q rows only)
   const int32_t* parents;  // [B, N]: a q row is needed only for nodes with a child
   spec_row_stats* stats_p;
   spec_row_stats* stats_q;
@@ -109,5 +110,13 @@ cudaError_t launch_philox_words(uint64_t seed, uint64_t offset, const int32_t* b
                                 const int32_t* node_idx, int32_t n, uint32_t* out,
                                 cudaStream_t s);
 int device_sm_count();
+
+// Fused LM head (lmhead.cu): bytes of the per-(row, column tile) statistics, and the
+// launch of the GEMM + statistics kernel and of the combine kernel that writes the
+// row statistics of the M target rows.
+size_t lmhead_part_bytes(int M, int V);
+cudaError_t launch_lmhead(const void* features, const void* weight, int M, int V, int K,
+                          float temperature, void* p, int64_t pitch, void* part, int* err,
+                          spec_row_stats* stats, unsigned long long* counters, cudaStream_t s);
 
 }  // namespace svk

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
     // ---------------- producer warp ----------------
     uint32_t g = 0;  // chunks issued so far (the same count the consumers walk)
     bool stop = false;
-    for (int v = blockIdx.x; v < total && !stop; v += gridDim.x) {
+    for (int v = job.first_row + (int)blockIdx.x; v < total && !stop; v += gridDim.x) {
       const char* row;
       if (job.mode == kRowsList) {
         row = static_cast<const char*>(row_ptr(job.base_p, (int64_t)v * job.row_pitch, Elt<T>::kBytes));
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
 
   // ---------------- consumer threads ----------------
   uint32_t g = 0;
-  for (int v = blockIdx.x; v < total; v += gridDim.x) {
+  for (int v = job.first_row + (int)blockIdx.x; v < total; v += gridDim.x) {
     const void* row;
     spec_row_stats* out;
     if (job.mode == kRowsList) {

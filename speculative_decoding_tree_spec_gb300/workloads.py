@@ -206,6 +206,28 @@ def make_lmhead_inputs(w: Workload, seed: int, device="cpu"):
     return feats, weight
 
 
+def build_lmhead_inputs(w: Workload, seed: int, device="cpu"):
+    """Inputs of the fused LM-head workload: features F [B*N, d], weight W [V, d], the
+    draft logits q [B, N, V] (bf16 of the fp32 product F W^T plus N(0, 1) noise, made
+    once here with torch.matmul), the tree and the draft tokens drawn from q."""
+    feats, weight = make_lmhead_inputs(w, seed, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) + 7919)
+    rows = w.B * w.N
+    Vp = padded_pitch(w.V, 2)
+    buf = torch.empty((rows, Vp), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, rows, 256):
+        r1 = min(rows, r0 + 256)
+        ref = torch.matmul(feats[r0:r1].float(), weight.float().t())
+        buf[r0:r1, :w.V] = (ref + torch.randn(ref.shape, generator=g, device=device)).to(
+            torch.bfloat16)
+    q = buf.view(w.B, w.N, Vp)[..., :w.V]
+    parents = make_parents(w, seed)
+    tokens = make_draft_tokens(w, q, parents, seed)
+    return {"features": feats, "weight": weight, "q": q, "parents": parents, "tokens": tokens,
+            "max_depth": tree_depth(parents), "workload": w}
+
+
 def make_draft_tokens(w: Workload, q: torch.Tensor, parents: np.ndarray, seed: int) -> np.ndarray:
     """[B, N] int32 draft tokens; entry 0 (root) is 0 and is never read.
 

@@ -1,0 +1,116 @@
+"""The fused LM head (spec_verify_tree_fused_lmhead): the target logits it computes on
+the tensor cores against torch.matmul with fp32 accumulation, rounded to bf16; and the
+verify outputs it gives against the oracle run on those same logits."""
+import numpy as np
+import pytest
+import torch
+
+from parity_helpers import compare, run_oracle
+from speculative_decoding_tree_spec_gb300 import binding
+from speculative_decoding_tree_spec_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+BASE = wl.WORKLOADS["lmhead_tree60_b32_v128256"]
+
+
+def _case(B, N, V, d, depth, temperature=0.8, top_p=0.9, top_k=0):
+    return BASE.with_(B=B, N=N, V=V, depth=depth, temperature=temperature, top_p=top_p,
+                      top_k=top_k, extra={"d": d, "w_std": 0.02})
+
+
+def _inputs(w, seed):
+    inp = wl.build_lmhead_inputs(w, seed, device=torch.device(DEV))
+    inp["tokens_d"] = torch.as_tensor(inp["tokens"], device=DEV)
+    inp["parents_d"] = torch.as_tensor(inp["parents"], device=DEV)
+    return inp
+
+
+def _run(w, inp, seed=11, **kw):
+    q = None if w.temperature == 0.0 else inp["q"]
+    out = binding.verify_tree_fused_lmhead(inp["features"], inp["weight"], q, inp["tokens_d"],
+                                           inp["parents_d"], inp["max_depth"], w.temperature,
+                                           w.top_k, w.top_p, seed=seed, want_counters=True, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check_logits(p, feats, weight, rows):
+    """p[rows] against the fp32 product rounded to bf16: within bf16 rounding of the
+    exact value (half an ulp, 2^-8 relative) plus the fp32 accumulation error."""
+    ref = torch.matmul(feats[rows].float(), weight.float().t())
+    got = p.reshape(-1, p.shape[-1])[rows].float()
+    err = (got - ref).abs()
+    bound = ref.abs() * (2.0 ** -8) + 1e-4
+    assert bool((err <= bound).all()), float((err - bound).max())
+    # nearly every element equals the rounded reference exactly (the tensor cores add
+    # the K products in another order, which moves values lying close to a bf16
+    # rounding boundary to the other side: about 0.2 % at K = 4096)
+    same = (got == ref.to(torch.bfloat16).float()).float().mean().item()
+    assert same > 0.99, same
+
+
+@pytest.mark.parametrize("B,N,V,d", [(2, 12, 3000, 256), (4, 60, 5003, 512), (1, 5, 256, 64)],
+                         ids=["ragged-m-n", "two-m-tiles", "single-tile"])
+def test_fused_logits_match_matmul(B, N, V, d):
+    w = _case(B, N, V, d, depth=min(4, N - 1))
+    inp = _inputs(w, 3)
+    out = _run(w, inp)
+    rows = torch.arange(B * N, device=DEV)
+    _check_logits(out["p"], inp["features"], inp["weight"], rows)
+    assert int(out["status"].max()) == 0
+
+
+@pytest.mark.parametrize("temperature,top_k,top_p", [(0.8, 0, 0.9), (1.0, 20, 0.95), (0.0, 0, 1.0),
+                                                     (0.6, 0, 1.0)],
+                         ids=["topp", "topk-topp", "greedy", "plain"])
+def test_fused_verify_matches_oracle(temperature, top_k, top_p):
+    w = _case(6, 40, 9000, 256, depth=5, temperature=temperature, top_k=top_k, top_p=top_p)
+    inp = _inputs(w, 5)
+    out = _run(w, inp, seed=17)
+    gpu = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in out.items() if k != "p"}
+    oinp = {"p": out["p"], "q": inp["q"], "tokens": inp["tokens"], "parents": inp["parents"],
+            "max_depth": inp["max_depth"]}
+    sel, outs = run_oracle(w, oinp, seed=17)
+    compared, excluded, _ = compare(w.with_(dtype="bf16"), gpu, sel, outs,
+                                    check_alpha=temperature > 0)
+    assert compared >= w.B - 1
+
+
+def test_fused_equals_verify_on_the_same_logits():
+    w = _case(8, 30, 7000, 128, depth=4)
+    inp = _inputs(w, 9)
+    fused = _run(w, inp, seed=23)
+    plain = binding.verify_tree(fused["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
+                                inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=23)
+    torch.cuda.synchronize()
+    for k in ("accept_len", "tokens", "path", "status"):
+        np.testing.assert_array_equal(fused[k].cpu().numpy(), plain[k].cpu().numpy(), err_msg=k)
+    a, b = fused["alpha"].cpu().numpy(), plain["alpha"].cpu().numpy()
+    np.testing.assert_array_equal(np.isnan(a), np.isnan(b))
+    m = ~np.isnan(a)
+    np.testing.assert_allclose(a[m], b[m], rtol=1e-5, atol=1e-7)
+
+
+def test_fused_full_size_sampled():
+    """The full workload (32 trees x 60 nodes, d 4096, V 128256): sampled logit rows
+    against matmul, and sampled trees against the oracle."""
+    w = BASE
+    inp = _inputs(w, 20261202)
+    out = _run(w, inp, seed=5)
+    rows = torch.arange(0, w.B * w.N, 97, device=DEV)
+    _check_logits(out["p"], inp["features"], inp["weight"], rows)
+    gpu = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in out.items() if k != "p"}
+    oinp = {"p": out["p"], "q": inp["q"], "tokens": inp["tokens"], "parents": inp["parents"],
+            "max_depth": inp["max_depth"]}
+    # the verify step on these logits: identical to spec_verify_tree on the same rows
+    plain = binding.verify_tree(out["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
+                                inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=5)
+    torch.cuda.synchronize()
+    for k in ("accept_len", "tokens", "path", "status"):
+        np.testing.assert_array_equal(gpu[k], plain[k].cpu().numpy(), err_msg=k)
+    # these logits are flat (std 1.28 at T = 0.8: near the top-p cut a token carries
+    # about 4e-6 of the mass), so most trees have a cut or a draw within the oracle's
+    # 1e-6 margin and are excluded; the trees that remain must match
+    sel, outs = run_oracle(w, oinp, trees=list(range(0, w.B, 4)), seed=5)
+    compare(w, gpu, sel, outs)

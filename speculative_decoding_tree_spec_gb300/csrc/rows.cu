@@ -859,12 +859,15 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
       // exact full-row selection
       SelOut rk{};
       const Eligible all{false, 0u, 0};
-      if (topk_on) rk = exact_select<T, CSync>(row, V, m, c, false, K, 0ull, all, sh.sel);
+      NoReduce one;
+      if (topk_on)
+        rk = exact_select<T, CSync>(row, V, m, c, false, K, 0ull, all, sh.sel, 0, nunits, one);
       if (topp_on) {
         const Eligible in_k{topk_on, rk.key, rk.idx};
         const unsigned long long tau = (unsigned long long)ceil(
             (double)job.top_p * (topk_on ? (double)rk.mass_kept : s_total * tau_scale));
-        const SelOut rp = exact_select<T, CSync>(row, V, m, c, true, 0u, tau, in_k, sh.sel);
+        const SelOut rp =
+            exact_select<T, CSync>(row, V, m, c, true, 0u, tau, in_k, sh.sel, 0, nunits, one);
         cut_key = rp.key; cut_idx = rp.idx; kept = rp.kept; sf_fixed = rp.mass_kept;
       } else {
         cut_key = rk.key; cut_idx = rk.idx; kept = rk.kept; sf_fixed = rk.mass_kept;

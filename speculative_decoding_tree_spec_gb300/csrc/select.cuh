@@ -8,6 +8,12 @@
 // top-k, exact 42-bit fixed-point mass for top-p) still reaches the target; it is
 // found by an 8-way split of the key range per pass over the row; ties inside K*
 // are cut in index order.  `Sync` names the barrier over the block's threads.
+//
+// Several blocks can share one row, each covering a contiguous slice of its units
+// [u_begin, u_end): `Red` then combines the blocks' tallies (integer counts and
+// fixed-point masses, so the totals are exact and every block takes the same
+// steps), the exclusive base of the tie count, and the tie index.  A row held by
+// one block uses NoReduce.
 #pragma once
 
 #include "common.cuh"
@@ -24,6 +30,16 @@ struct SelShared {
   unsigned long long red_mass[8];
   unsigned red_min;
   int tie_idx;
+};
+
+// The combination step of a row held by a single block: nothing to combine.
+struct NoReduce {
+  __device__ void tally(SelShared&) {}
+  __device__ void base(unsigned mine, unsigned& base, unsigned& total) {
+    base = 0;
+    total = mine;
+  }
+  __device__ int max_int(int v) { return v; }
 };
 
 // Block-wide exclusive scan of (count, mass) pairs; also returns the totals.
@@ -85,19 +101,18 @@ struct SelOut {
 // Results land in sh.red_cnt / sh.red_mass / sh.red_min.
 constexpr int kSplit = 7;  // thresholds per pass: an 8-way split of the key range
 
-template <typename T, class Sync>
+template <typename T, class Sync, class Red>
 __device__ void tally_range(const void* row, int V, float m, float c, int ks,
                             const uint32_t (&th)[kSplit], uint32_t hi, const Eligible& elig,
-                            SelShared& sh) {
+                            SelShared& sh, int u_begin, int u_end, Red& red) {
   constexpr int E = Elt<T>::kPerUnit;
-  const int nunits = (V + E - 1) / E;
   const int lane = threadIdx.x & 31;
   unsigned cnt[kSplit];
   unsigned long long mass[kSplit];
 #pragma unroll
   for (int t = 0; t < kSplit; ++t) { cnt[t] = 0; mass[t] = 0; }
   unsigned kmin = 0xffffffffu;
-  for (int u = threadIdx.x; u < nunits; u += kSelThreads) {
+  for (int u = u_begin + (int)threadIdx.x; u < u_end; u += kSelThreads) {
     float f[E];
     load_unit<T>(row, V, u, f);
 #pragma unroll
@@ -137,16 +152,16 @@ __device__ void tally_range(const void* row, int V, float m, float c, int ks,
     atomicMin(&sh.red_min, kmin);
   }
   Sync::sync();
+  red.tally(sh);
 }
 
 // The j-th (1-based) eligible token with order key `key`, in index order.
-template <typename T, class Sync>
+template <typename T, class Sync, class Red>
 __device__ int tie_cut(const void* row, int V, uint32_t key, unsigned j, const Eligible& elig,
-                       SelShared& sh) {
+                       SelShared& sh, int u_begin, int u_end, Red& red) {
   constexpr int E = Elt<T>::kPerUnit;
-  const int nunits = (V + E - 1) / E;
-  const int per = (nunits + kSelThreads - 1) / kSelThreads;
-  const int u_lo = threadIdx.x * per, u_hi = min(nunits, u_lo + per);
+  const int per = (u_end - u_begin + kSelThreads - 1) / kSelThreads;
+  const int u_lo = min(u_end, u_begin + (int)threadIdx.x * per), u_hi = min(u_end, u_lo + per);
   unsigned mine = 0;
   for (int u = u_lo; u < u_hi; ++u) {
     float f[E];
@@ -163,6 +178,9 @@ __device__ int tie_cut(const void* row, int V, uint32_t key, unsigned j, const E
   unsigned base, tot;
   unsigned long long bw, tw;
   block_exscan<Sync>(mine, 0ull, base, bw, tot, tw, sh);
+  unsigned cbase, ctot;
+  red.base(tot, cbase, ctot);  // tokens of the blocks before this one
+  base += cbase;
   if (threadIdx.x == 0) sh.tie_idx = -1;
   Sync::sync();
   if (base < j && base + mine >= j) {
@@ -181,13 +199,13 @@ __device__ int tie_cut(const void* row, int V, uint32_t key, unsigned j, const E
     }
   }
   Sync::sync();
-  return sh.tie_idx;
+  return red.max_int(sh.tie_idx);
 }
 
-template <typename T, class Sync>
+template <typename T, class Sync, class Red>
 __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by_mass,
                                unsigned need_count, uint64_t need_mass, Eligible elig,
-                               SelShared& sh) {
+                               SelShared& sh, int u_begin, int u_end, Red& red) {
   const int ks = (sizeof(T) == 2) ? 16 : 0;  // bf16 keys carry 16 constant low bits
   const uint32_t kmax = order_key(m) >> ks;
   auto reaches = [&](unsigned cnt, unsigned long long mass) {
@@ -196,7 +214,7 @@ __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by
   // first pass: eligible totals and the smallest eligible key
   uint32_t th[kSplit];
   for (int t = 0; t < kSplit; ++t) th[t] = 0u;
-  tally_range<T, Sync>(row, V, m, c, ks, th, 0xffffffffu, elig, sh);
+  tally_range<T, Sync, Red>(row, V, m, c, ks, th, 0xffffffffu, elig, sh, u_begin, u_end, red);
   uint64_t lo = sh.red_min, hi = kmax;
   // tokens with a key above hi: their count and mass, carried from pass to pass
   unsigned above_c = 0;
@@ -209,7 +227,7 @@ __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by
     const uint64_t span = hi - lo;
     for (int t = 0; t < kSplit; ++t)
       th[t] = (uint32_t)(lo + (span * (uint64_t)(t + 1) + kSplit) / (kSplit + 1));
-    tally_range<T, Sync>(row, V, m, c, ks, th, (uint32_t)hi, elig, sh);
+    tally_range<T, Sync, Red>(row, V, m, c, ks, th, (uint32_t)hi, elig, sh, u_begin, u_end, red);
     int pick = -1;
     for (int t = kSplit - 1; t >= 0; --t)
       if (reaches(above_c + sh.red_cnt[t], above_m + sh.red_mass[t])) { pick = t; break; }
@@ -229,7 +247,7 @@ __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by
   // the tokens carrying the cut key
   const uint32_t kstar = (uint32_t)lo;
   for (int t = 0; t < kSplit; ++t) th[t] = kstar;
-  tally_range<T, Sync>(row, V, m, c, ks, th, kstar, elig, sh);
+  tally_range<T, Sync, Red>(row, V, m, c, ks, th, kstar, elig, sh, u_begin, u_end, red);
   const unsigned cnt_eq = sh.red_cnt[0];
   const unsigned long long w_eq = cnt_eq ? sh.red_mass[0] / cnt_eq : 0ull;
   unsigned j;
@@ -249,7 +267,7 @@ __device__ SelOut exact_select(const void* row, int V, float m, float c, bool by
   const uint32_t key = ks ? key_from16(kstar) : kstar;
   SelOut r;
   r.key = key;
-  r.idx = tie_cut<T, Sync>(row, V, key, j, elig, sh);
+  r.idx = tie_cut<T, Sync, Red>(row, V, key, j, elig, sh, u_begin, u_end, red);
   r.kept = above_c + j;
   r.mass_kept = above_m + w_eq * j;
   return r;

@@ -36,7 +36,7 @@ constexpr int CW = CT / 32;
 constexpr int kMaxC = kMaxWalkCluster;
 constexpr int kUnitsInFlight = 2;          // units of each row a thread loads before using them
 constexpr uint64_t kExchangeLimitNs = 2000000000ull;
-constexpr int kSlotW = 4;      // 64-bit words one CTA can push in one exchange
+constexpr int kSlotW = 16;     // 64-bit words one CTA can push in one exchange
 constexpr int kCandCTA = 512;  // window candidates one CTA keeps per row
 constexpr int kSortW = 2048;   // largest window (per row) the walk resolves by sorting
 constexpr int kSortPer = kSortW / CT;
@@ -811,26 +811,6 @@ __device__ bool window_cut(const uint64_t* keys, unsigned n, unsigned n_pad, flo
   return true;
 }
 
-// The exact selection of one row by this CTA alone (the dense row pass's rule).
-template <typename T>
-__device__ RowCut exact_cut(const void* row, int V, float m, float c, double s_all,
-                            const TreeJob& job, CShared& sh) {
-  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
-  SelOut rk{};
-  const Eligible all{false, 0u, 0};
-  if (topk_on) rk = exact_select<T, BSync>(row, V, m, c, false, (unsigned)job.top_k, 0ull, all, sh.sel);
-  RowCut out;
-  if (topp_on) {
-    const Eligible in_k{topk_on, rk.key, rk.idx};
-    const unsigned long long tau = (unsigned long long)ceil(
-        (double)job.top_p * (topk_on ? (double)rk.mass_kept : s_all * 4398046511104.0));
-    const SelOut rp = exact_select<T, BSync>(row, V, m, c, true, 0u, tau, in_k, sh.sel);
-    out.key = rp.key; out.idx = rp.idx; out.kept = rp.kept; out.mass = rp.mass_kept;
-  } else {
-    out.key = rk.key; out.idx = rk.idx; out.kept = rk.kept; out.mass = rk.mass_kept;
-  }
-  return out;
-}
 
 __device__ __forceinline__ void set_cut(spec_row_stats& s, const RowCut& rc) {
   s.cut_key = rc.key;
@@ -839,26 +819,99 @@ __device__ __forceinline__ void set_cut(spec_row_stats& s, const RowCut& rc) {
   s.s_f = fixed_to_double(rc.mass);
 }
 
-// The exact selection of one row on CTA 0, shared with the cluster.
-template <typename T>
-__device__ bool shared_exact_cut(const TreeJob& job, const void* row, const spec_row_stats& s,
-                                 CShared& sh, int C, uint32_t rank, uint32_t& n_ex, float c,
-                                 RowCut& rc) {
-  uint64_t w[3] = {0ull, 0ull, 0ull};
-  if (rank == 0) {
-    const RowCut ex = exact_cut<T>(row, job.V, s.m, c, s.s_f, job, sh);
-    w[0] = (uint64_t)ex.key | ((uint64_t)(uint32_t)ex.idx << 32);
-    w[1] = ex.kept;
-    w[2] = ex.mass;
-    if (threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[5], 1ull);
+// The exact selection's combination step over a cluster: every CTA tallies its own
+// slice and the tallies are exchanged and summed in rank order (integers: the same
+// totals everywhere).  `ok` drops when an exchange gives up.
+struct ClusterReduce {
+  CShared* sh;
+  int C;
+  uint32_t rank;
+  uint32_t* n_ex;
+  bool ok;
+  __device__ void tally(SelShared& s) {
+    uint64_t w[2 * kSplit + 1];
+    for (int t = 0; t < kSplit; ++t) {
+      w[t] = s.red_cnt[t];
+      w[kSplit + t] = s.red_mass[t];
+    }
+    w[2 * kSplit] = s.red_min;
+    const SlotRow* sl = cluster_share(w, 2 * kSplit + 1, *sh, C, rank, *n_ex);
+    if (!sl) {
+      ok = false;
+      return;
+    }
+    unsigned cnt[kSplit];
+    unsigned long long mass[kSplit];
+    unsigned mn = 0xffffffffu;
+    for (int t = 0; t < kSplit; ++t) { cnt[t] = 0u; mass[t] = 0ull; }
+    for (int q = 0; q < C; ++q) {
+      for (int t = 0; t < kSplit; ++t) {
+        cnt[t] += (unsigned)sl[q][t];
+        mass[t] += sl[q][kSplit + t];
+      }
+      mn = min(mn, (unsigned)sl[q][2 * kSplit]);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int t = 0; t < kSplit; ++t) { s.red_cnt[t] = cnt[t]; s.red_mass[t] = mass[t]; }
+      s.red_min = mn;
+    }
+    __syncthreads();
   }
-  const SlotRow* x = cluster_share(w, 3, sh, C, rank, n_ex);
-  if (!x) return false;
-  rc.key = (uint32_t)x[0][0];
-  rc.idx = (int)(uint32_t)(x[0][0] >> 32);
-  rc.kept = (unsigned)x[0][1];
-  rc.mass = x[0][2];
-  return true;
+  __device__ void base(unsigned mine, unsigned& b, unsigned& total) {
+    const uint64_t w = mine;
+    const SlotRow* sl = cluster_share(&w, 1, *sh, C, rank, *n_ex);
+    b = 0u;
+    total = mine;
+    if (!sl) {
+      ok = false;
+      return;
+    }
+    total = 0u;
+    for (int q = 0; q < C; ++q) {
+      if (q < (int)rank) b += (unsigned)sl[q][0];
+      total += (unsigned)sl[q][0];
+    }
+  }
+  __device__ int max_int(int v) {
+    const uint64_t w = (uint64_t)(uint32_t)(v + 1);  // -1 (not found here) -> 0
+    const SlotRow* sl = cluster_share(&w, 1, *sh, C, rank, *n_ex);
+    if (!sl) {
+      ok = false;
+      return v;
+    }
+    int mx = 0;
+    for (int q = 0; q < C; ++q) mx = max(mx, (int)(uint32_t)sl[q][0]);
+    return mx - 1;
+  }
+};
+
+// The exact selection of one row by the whole cluster (each CTA over its slice of
+// units [ua, ub)): the dense row pass's rule, the same result.
+template <typename T>
+__device__ bool cluster_exact_cut(const TreeJob& job, const void* row, const spec_row_stats& s,
+                                  int ua, int ub, CShared& sh, int C, uint32_t rank,
+                                  uint32_t& n_ex, float c, RowCut& out) {
+  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
+  const int V = job.V;
+  ClusterReduce red{&sh, C, rank, &n_ex, true};
+  SelOut rk{};
+  const Eligible all{false, 0u, 0};
+  if (topk_on)
+    rk = exact_select<T, BSync>(row, V, s.m, c, false, (unsigned)job.top_k, 0ull, all, sh.sel,
+                                ua, ub, red);
+  if (topp_on) {
+    const Eligible in_k{topk_on, rk.key, rk.idx};
+    const unsigned long long tau = (unsigned long long)ceil(
+        (double)job.top_p * (topk_on ? (double)rk.mass_kept : s.s_f * 4398046511104.0));
+    const SelOut rp = exact_select<T, BSync>(row, V, s.m, c, true, 0u, tau, in_k, sh.sel, ua,
+                                             ub, red);
+    out.key = rp.key; out.idx = rp.idx; out.kept = rp.kept; out.mass = rp.mass_kept;
+  } else {
+    out.key = rk.key; out.idx = rk.idx; out.kept = rk.kept; out.mass = rk.mass_kept;
+  }
+  if (rank == 0 && threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[5], 1ull);
+  return red.ok;
 }
 
 // The cut of the p row (and of the q row when with_q) of node u, written into the
@@ -938,7 +991,8 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
     RowCut rc{};
     bool ok = fast[r] && window_cut(sortb + r * kSortW, total[r], n_pad[r], s.m, c, s.s_f, job,
                                     sh, rc);
-    if (!ok && !shared_exact_cut<T>(job, rows[r], s, sh, C, rank, n_ex, c, rc)) return false;
+    if (!ok && !cluster_exact_cut<T>(job, rows[r], s, ua, ub, sh, C, rank, n_ex, c, rc))
+      return false;
     set_cut(s, rc);
   }
   return true;
@@ -1252,7 +1306,8 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   for (int r = 0; r < nrows; ++r) {
     if (ok[r]) continue;
     RowCut rc;
-    if (!shared_exact_cut<uint16_t>(job, rows[r], *st[r], sh, C, rank, n_ex, c, rc)) return false;
+    if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, c, rc))
+      return false;
     set_cut(*st[r], rc);
   }
   return true;

@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--cpu-trees", type=int, default=48,
                     help="tree-steps in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--visited-only", action="store_true",
+                    help="the visited-rows-only schedule (no dense pass); reported as its own "
+                         "line, not the dense schedule's number")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -293,8 +296,9 @@ def run_ours(args):
     inp = wl.build_inputs(w, seed=seed, device=dev)
     tok = torch.as_tensor(inp["tokens"], device=dev)
     par = torch.as_tensor(inp["parents"], device=dev)
+    flags = binding.SPEC_FLAG_VISITED_ONLY if args.visited_only else 0
     call = binding.PreparedVerify(inp["p"], inp["q"], tok, par, inp["max_depth"], w.temperature,
-                                  w.top_k, w.top_p, seed=seed, offset=0)
+                                  w.top_k, w.top_p, seed=seed, offset=0, flags=flags)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         call()
@@ -335,16 +339,27 @@ def run_ours(args):
 
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    achieved = counters["dense_bytes"] / (row_avg_ms / 1e3) / 1e9
-    traffic, traffic_state = profiled_traffic(w.name)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": "row_pass_kernel (dense row pass)",
-                "peak_source": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": counters["dense_bytes"],
-                "avg_launch_ms": row_avg_ms}
-    if traffic_state == "stale":
-        roofline["traffic_note"] = "ncu capture predates the current row-pass sources"
+    if args.visited_only:
+        # no dense pass: the walk is the only kernel; its rows read over its time
+        walk_ms = ms_per_step - row_avg_ms
+        achieved = counters["walk_bytes"] / (walk_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": None,
+                    "kernel": "cluster_walk_kernel (visited rows only; latency-bound)",
+                    "peak_source": f"{peak_kind} hbm_gbs",
+                    "algorithmic_bytes_per_launch": counters["walk_bytes"],
+                    "avg_launch_ms": walk_ms}
+    else:
+        achieved = counters["dense_bytes"] / (row_avg_ms / 1e3) / 1e9
+        traffic, traffic_state = profiled_traffic(w.name)
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": traffic,
+                    "kernel": "row_pass_kernel (dense row pass)",
+                    "peak_source": f"{peak_kind} hbm_gbs",
+                    "algorithmic_bytes_per_launch": counters["dense_bytes"],
+                    "avg_launch_ms": row_avg_ms}
+        if traffic_state == "stale":
+            roofline["traffic_note"] = "ncu capture predates the current row-pass sources"
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -356,6 +371,8 @@ def run_ours(args):
                    "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
                    "tree": f"{w.tree}, depth {inp['max_depth']}, branching <= {w.max_branch}",
                    "rng_offset": "fixed per step",
+                   "schedule": ("visited rows only (no dense pass)" if args.visited_only
+                                else "dense pass over every row"),
                    "l2": f"inputs {2 * w.B * w.N * w.V * (2 if w.dtype == 'bf16' else 4) / 1e9:.2f}"
                          " GB per step, larger than L2; no flush",
                    "parallelism": f"weak: {world} rank(s) x {w.B} trees"},
@@ -363,7 +380,7 @@ def run_ours(args):
         "step_hbm_gbs": (counters["dense_bytes"] + counters["walk_bytes"]) / (ms_per_step / 1e3) / 1e9,
         "work_per_step": counters,
         "roofline": roofline,
-        "gpu_launches": 2 * K,  # row_pass_kernel + tree_walk_kernel per step
+        "gpu_launches": (1 if args.visited_only else 2) * K,  # [row pass +] walk per step
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
 
@@ -502,8 +519,10 @@ def run_e2e(args, w, inp, dev, stream):
     host["tokens"] = torch.as_tensor(inp["tokens"]).pin_memory()
     host["parents"] = torch.as_tensor(inp["parents"]).pin_memory()
     dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    flags = binding.SPEC_FLAG_VISITED_ONLY if args.visited_only else 0
     call = binding.PreparedVerify(dbuf["p"], dbuf["q"], dbuf["tokens"], dbuf["parents"],
-                                  inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=1, offset=0)
+                                  inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=1, offset=0,
+                                  flags=flags)
     outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
             for k, v in call.out.items() if k in ("accept_len", "tokens", "path")}
     h2d = sum(v.numel() * v.element_size() for v in host.values())

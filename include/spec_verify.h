@@ -71,6 +71,12 @@ typedef struct {
  * wait on it expires (after 20 ms); the affected rows report SPEC_ROW_TIMEOUT and
  * the call still completes. */
 #define SPEC_FLAG_TEST_STALL 2u
+/* Visited-rows-only schedule (spec_verify_tree and its variants): no dense pass over
+ * all B * N rows; the walk computes the statistics (maximum, sum, argmax) of the p
+ * and q rows of the nodes it visits, so a step reads about B * (accepted depth + 1)
+ * row pairs instead of every row.  Same results.  Ignored by the fused LM-head call,
+ * which computes every target row. */
+#define SPEC_FLAG_VISITED_ONLY 4u
 
 /* Return codes. */
 #define SPEC_OK 0

@@ -22,6 +22,7 @@ SPEC_F32 = 0
 SPEC_BF16 = 1
 SPEC_FLAG_EXACT_SELECT = 1
 SPEC_FLAG_TEST_STALL = 2
+SPEC_FLAG_VISITED_ONLY = 4
 SPEC_TREE_OK = 0
 SPEC_ROW_NONFINITE = 1
 SPEC_TREE_INVALID = 2

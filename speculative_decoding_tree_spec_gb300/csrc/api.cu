@@ -30,7 +30,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_params(const spec_sampling_params& prm) {
   if (!std::isfinite(prm.temperature) || prm.temperature < 0.0f) return SPEC_ERR_INVALID_ARG;
   if (!(prm.top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;  // also rejects NaN
-  if (prm.flags & ~(SPEC_FLAG_EXACT_SELECT | SPEC_FLAG_TEST_STALL)) return SPEC_ERR_INVALID_ARG;
+  if (prm.flags & ~(SPEC_FLAG_EXACT_SELECT | SPEC_FLAG_TEST_STALL | SPEC_FLAG_VISITED_ONLY))
+    return SPEC_ERR_INVALID_ARG;
   return SPEC_OK;
 }
 
@@ -127,6 +128,7 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   tj.trunc = (!greedy && (tj.top_k > 0 || tj.top_p < 1.0f)) ? 1 : 0;
   tj.delta_z = kWindowNats * params.temperature;
   tj.exact = (params.flags & SPEC_FLAG_EXACT_SELECT) ? 1 : 0;
+  tj.visited_only = (params.flags & SPEC_FLAG_VISITED_ONLY) ? 1 : 0;
   tj.seed = rng_seed;
   tj.offset = rng_offset;
   tj.out_accept_len = out_accept_len;
@@ -158,7 +160,9 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   rj.stats_q = stats_q;
   rj.counters = tj.counters;
   const int virtual_rows = B * N * (greedy ? 1 : 2);
-  if ((phases & SPEC_PHASE_ROWS) && launch_row_pass(rj, dtype, virtual_rows, s) != cudaSuccess)
+  // the visited-rows-only schedule has no dense pass
+  if ((phases & SPEC_PHASE_ROWS) && !tj.visited_only &&
+      launch_row_pass(rj, dtype, virtual_rows, s) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   if (phases & SPEC_PHASE_WALK) {

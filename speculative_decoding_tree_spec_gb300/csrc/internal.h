@@ -94,6 +94,7 @@ struct TreeJob {
   float top_p;        // 1 = off
   float delta_z;      // candidate window below the row maximum (logit units)
   int32_t exact;      // always take the full-row exact selection
+  int32_t visited_only;  // no dense pass: the walk computes the statistics of the rows it visits
   uint64_t seed, offset;
   int32_t* out_accept_len;
   int32_t* out_tokens;

@@ -140,34 +140,82 @@ __device__ void finish_tree(const TreeJob& job, int b, int status, int n_acc, in
 // ---------------------------------------------------------------------------
 // Greedy walk: one block per tree; decisions come from the row argmax alone.
 // ---------------------------------------------------------------------------
+// Argmax of one row by the whole block (visited-rows-only schedule): the lowest index
+// of the maximum, and whether the row is not finite (NaN, +inf, or all -inf).
+template <typename T>
+__device__ void block_argmax(const void* row, int V, int& arg, int& status, float* red_m,
+                             int* red_i) {
+  constexpr int E = Elt<T>::kPerUnit;
+  const int nunits = (V + E - 1) / E;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float m = -CUDART_INF_F;
+  int idx = INT_MAX, bad = 0;
+  for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+    float z[E];
+    load_unit<T>(row, V, u, z);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      bad |= (z[e] != z[e]);
+      if (z[e] > m) { m = z[e]; idx = u * E + e; }
+    }
+  }
+  const float wm = warp_max(m);
+  const int wi = warp_min_i(m == wm ? idx : INT_MAX);
+  bad = __syncthreads_or(bad);
+  if (lane == 0) { red_m[warp] = wm; red_i[warp] = wi; }
+  __syncthreads();
+  float bm = -CUDART_INF_F;
+  int bi = INT_MAX;
+  for (int q = 0; q < (int)(blockDim.x >> 5); ++q) bm = fmaxf(bm, red_m[q]);
+  for (int q = 0; q < (int)(blockDim.x >> 5); ++q)
+    if (red_m[q] == bm) bi = min(bi, red_i[q]);
+  __syncthreads();
+  arg = (bi == INT_MAX) ? 0 : bi;
+  status = (bad || bm == CUDART_INF_F || bm == -CUDART_INF_F) ? SPEC_ROW_NONFINITE : SPEC_TREE_OK;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(GT) greedy_walk_kernel(TreeJob job) {
   __shared__ int s_status;
+  __shared__ float red_m[GT / 32];
+  __shared__ int red_i[GT / 32];
   extern __shared__ __align__(16) int32_t tsm[];
   const int b = blockIdx.x;
   const int N = job.N;
   int32_t *par = tsm, *tok = tsm + N, *cs = tsm + 2 * N, *cl = tsm + 3 * N + 1;
   int status = load_tree(job, b, par, tok, cs, cl, true, &s_status);
-  if (threadIdx.x != 0) return;
   int32_t* out_tok = job.out_tokens + (int64_t)b * job.W;
   int32_t* out_path = job.out_path + (int64_t)b * job.W;
   int u = 0, n_acc = 0, final_tok = -1;
   while (status == SPEC_TREE_OK) {
-    const spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
-    if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
+    int argmax, st;
+    if (job.visited_only) {
+      block_argmax<T>(row_at(job.base_p, job, b, u, Elt<T>::kBytes), job.V, argmax, st, red_m,
+                      red_i);
+      if (threadIdx.x == 0 && job.counters)
+        atomicAdd(&job.counters[2], (unsigned long long)job.V * Elt<T>::kBytes);
+    } else {
+      const spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
+      argmax = sp.argmax;
+      st = sp.status;
+    }
+    if (st != SPEC_TREE_OK) { status = st; break; }
     int next = -1;
     for (int i = cs[u]; i < cs[u + 1]; ++i) {
       const int ch = cl[i];
-      const bool ok = tok[ch] == sp.argmax;
-      if (job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = ok ? 1.f : 0.f;
+      const bool ok = tok[ch] == argmax;
+      if (threadIdx.x == 0 && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = ok ? 1.f : 0.f;
       if (ok) { next = ch; break; }
     }
-    if (next < 0) { final_tok = sp.argmax; break; }
-    out_tok[n_acc] = tok[next];
-    out_path[n_acc + 1] = next;
+    if (next < 0) { final_tok = argmax; break; }
+    if (threadIdx.x == 0) {
+      out_tok[n_acc] = tok[next];
+      out_path[n_acc + 1] = next;
+    }
     ++n_acc;
     u = next;
   }
-  finish_tree(job, b, status, n_acc, final_tok, true);
+  if (threadIdx.x == 0) finish_tree(job, b, status, n_acc, final_tok, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -422,6 +470,11 @@ struct CShared {
   uint32_t kid_k[2][kPreKids];
   double kid_u[kPreKids];
   int tie_max[2], tie_idx[2];
+  // visited-rows-only schedule: per-warp row statistics of the cluster's stats pass
+  float st_m[2][CW];
+  double st_s[2][CW];
+  int st_arg[2][CW];
+  int st_bad[2];
   SelShared sel;
 };
 
@@ -1313,6 +1366,132 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   return true;
 }
 
+// Visited-rows-only schedule: the statistics the dense row pass would have written
+// for the p row (and the q row when with_q) of a node the walk visits, computed by
+// the cluster.  Every CTA covers its slice with a running maximum (its first index)
+// and the Kahan sum of 2^((z - max) c), referred to the warp's maximum, then to the
+// CTA's; the CTAs' (maximum, sum, argmax, NaN) are exchanged and combined in rank
+// order, so every CTA holds the same statistics.
+template <typename T>
+__device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const void* qrow,
+                                  bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
+                                  int ub, CShared& sh, int C, uint32_t rank, uint32_t& n_ex,
+                                  float c) {
+  constexpr int E = Elt<T>::kPerUnit;
+  const int V = job.V;
+  const int nrows = with_q ? 2 : 1;
+  const void* const rows[2] = {prow, qrow};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float tm[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  int targ[2] = {INT_MAX, INT_MAX};
+  Kahan ks[2];
+  int bad[2] = {0, 0};
+  if (threadIdx.x < 2) sh.st_bad[threadIdx.x] = 0;
+  __syncthreads();
+  for (int u = ua + (int)threadIdx.x; u < ub; u += CT) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
+      float z[E];
+      load_unit<T>(rows[r], V, u, z);
+      float um = z[0];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        bad[r] |= (z[e] != z[e]);
+        um = fmaxf(um, z[e]);
+      }
+      if (um > tm[r]) {
+        int first = E - 1;
+#pragma unroll
+        for (int e = E - 1; e >= 0; --e)
+          if (z[e] == um) first = e;
+        targ[r] = u * E + first;
+        if (tm[r] != -CUDART_INF_F) {
+          const float scale = ex2_approx((tm[r] - um) * c);
+          ks[r].s *= scale;
+          ks[r].c *= scale;
+        }
+        tm[r] = um;
+      }
+      if (tm[r] != -CUDART_INF_F) {
+        float part = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) part += tempered_weight(z[e], tm[r], c);
+        ks[r].add(part);
+      }
+    }
+  }
+  for (int r = 0; r < nrows; ++r) {
+    const float wm = warp_max(tm[r]);
+    FF sv = ks[r].ff();
+    if (tm[r] != -CUDART_INF_F && tm[r] != wm) {
+      const float scale = ex2_approx((tm[r] - wm) * c);
+      sv.hi *= scale;
+      sv.lo *= scale;
+    }
+    const FF ws = warp_sum_ff(sv);
+    const int warg = warp_min_i(tm[r] == wm ? targ[r] : INT_MAX);
+    const int wbad = __any_sync(kFull, bad[r]);
+    if (lane == 0) {
+      sh.st_m[r][warp] = wm;
+      sh.st_s[r][warp] = ws.value();
+      sh.st_arg[r][warp] = warg;
+      if (wbad) atomicOr(&sh.st_bad[r], 1);
+    }
+  }
+  __syncthreads();
+  uint64_t w[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < nrows; ++r) {
+      float m = -CUDART_INF_F;
+      for (int q = 0; q < CW; ++q) m = fmaxf(m, sh.st_m[r][q]);
+      double s = 0.0;
+      int arg = INT_MAX;
+      for (int q = 0; q < CW; ++q) {
+        if (sh.st_m[r][q] != -CUDART_INF_F)
+          s += sh.st_s[r][q] * (double)exp2f((sh.st_m[r][q] - m) * c);
+        if (sh.st_m[r][q] == m) arg = min(arg, sh.st_arg[r][q]);
+      }
+      w[4 * r + 0] = (uint64_t)__float_as_uint(m);
+      w[4 * r + 1] = (uint64_t)__double_as_longlong(s);
+      w[4 * r + 2] = (uint64_t)(uint32_t)arg;
+      w[4 * r + 3] = (uint64_t)sh.st_bad[r];
+    }
+  }
+  const SlotRow* sl = cluster_share(w, 4 * nrows, sh, C, rank, n_ex);
+  if (!sl) return false;
+  spec_row_stats* st[2] = {&sp, &sq};
+  for (int r = 0; r < nrows; ++r) {
+    float m = -CUDART_INF_F;
+    int any_bad = 0;
+    for (int q = 0; q < C; ++q) {
+      m = fmaxf(m, __uint_as_float((uint32_t)sl[q][4 * r]));
+      any_bad |= (int)sl[q][4 * r + 3];
+    }
+    double s = 0.0;
+    int arg = INT_MAX;
+    for (int q = 0; q < C; ++q) {
+      const float mq = __uint_as_float((uint32_t)sl[q][4 * r]);
+      if (mq != -CUDART_INF_F)
+        s += __longlong_as_double((long long)sl[q][4 * r + 1]) * (double)exp2f((mq - m) * c);
+      if (mq == m) arg = min(arg, (int)(uint32_t)sl[q][4 * r + 2]);
+    }
+    const bool finite = !any_bad && m != CUDART_INF_F && m != -CUDART_INF_F && s == s &&
+                        s != CUDART_INF;
+    spec_row_stats& o = *st[r];
+    o.m = m;
+    o.status = finite ? SPEC_TREE_OK : SPEC_ROW_NONFINITE;
+    o.s_f = s;
+    o.cut_key = 0u;
+    o.cut_idx = V - 1;
+    o.argmax = (arg == INT_MAX) ? 0 : arg;
+    o.kept = V;
+  }
+  if (rank == 0 && threadIdx.x == 0 && job.counters)
+    atomicAdd(&job.counters[2], (unsigned long long)nrows * V * Elt<T>::kBytes);
+  return true;
+}
+
 template <typename T>
 __device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qrow, bool with_q,
                             spec_row_stats& sp, spec_row_stats& sq, int ua, int ub,
@@ -1382,16 +1561,25 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   int u = 0, n_acc = 0, final_tok = -1, owner = -1;
 
   while (status == SPEC_TREE_OK) {
-    spec_row_stats sp = job.stats_p[(int64_t)b * N + u];
-    if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
     const int c0 = cs[u], c1 = cs[u + 1];
     const void* prow = row_at(job.base_p, job, b, u, Elt<T>::kBytes);
     const void* qrow = row_at(job.base_q, job, b, u, Elt<T>::kBytes);
-    spec_row_stats sq = sp;
-    if (c1 > c0) {
-      sq = job.stats_q[(int64_t)b * N + u];
-      if (sq.status != SPEC_TREE_OK) { status = sq.status; break; }
+    spec_row_stats sp, sq;
+    if (job.visited_only) {
+      // no dense pass: the statistics of this node's rows come from the cluster
+      if (!cluster_row_stats<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, sh, C, rank, n_ex, c)) {
+        timed_out = true;
+        status = SPEC_ROW_TIMEOUT;
+        break;
+      }
+      if (c1 == c0) sq = sp;
+    } else {
+      sp = job.stats_p[(int64_t)b * N + u];
+      sq = sp;
+      if (c1 > c0 && sp.status == SPEC_TREE_OK) sq = job.stats_q[(int64_t)b * N + u];
     }
+    if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
+    if (c1 > c0 && sq.status != SPEC_TREE_OK) { status = sq.status; break; }
     // the first children's accept-test inputs, one lane per (child, row) of warp 0;
     // they do not depend on the cut and overlap the rest of the block's work
     const int n_pre = min(c1 - c0, kPreKids);
@@ -1505,14 +1693,15 @@ __global__ void philox_words_kernel(uint64_t seed, uint64_t offset, const int32_
 
 size_t tree_smem_bytes(int N) { return (size_t)((4 * N + 1 + 1) & ~1) * sizeof(int32_t); }
 
+template <typename T>
 cudaError_t launch_greedy(const TreeJob& job, cudaStream_t s) {
   const size_t dyn = tree_smem_bytes(job.N);
   if (dyn > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
-        greedy_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        greedy_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
   }
-  greedy_walk_kernel<<<job.B, GT, dyn, s>>>(job);
+  greedy_walk_kernel<T><<<job.B, GT, dyn, s>>>(job);
   return cudaGetLastError();
 }
 
@@ -1565,7 +1754,8 @@ cudaError_t launch_sampling(const TreeJob& job, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, cudaStream_t s) {
-  if (greedy) return launch_greedy(job, s);
+  if (greedy)
+    return dtype == SPEC_BF16 ? launch_greedy<uint16_t>(job, s) : launch_greedy<float>(job, s);
   if (dtype == SPEC_BF16) return launch_sampling<uint16_t>(job, s);
   return launch_sampling<float>(job, s);
 }

@@ -98,7 +98,7 @@ def _call(L, **kw):
     (dict(params=binding.params(float("inf"))), -1),
     (dict(params=binding.params(0.7, 0, 0.0)), -1),
     (dict(params=binding.params(0.7, 0, float("nan"))), -1),
-    (dict(params=binding.params(0.7, 0, 0.9, flags=4)), -1),
+    (dict(params=binding.params(0.7, 0, 0.9, flags=8)), -1),
     (dict(logits_p=None), -1),
     (dict(logits_q=None), -1),
     (dict(draft_tokens=None), -1),

@@ -343,3 +343,35 @@ def test_chi_squared_first_token_on_gpu():
     m = P0 > 0
     assert obs[~m].sum() == 0
     assert stats.chisquare(obs[m], P0[m] * B).pvalue > 1e-3
+
+
+# --- visited-rows-only schedule (no dense pass) -----------------------------------
+
+@pytest.mark.parametrize("w", [
+    W["tree60_b64_v128256"].with_(B=6),
+    W["tree26_b256_v152064"].with_(B=6),
+    W["tree60_b64_v128256"].with_(B=6, dtype="f32", V=32000),
+    W["tree26_b256_v152064"].with_(B=6, temperature=0.0),
+    W["tree60_b64_v128256"].with_(B=8, N=40, V=5003, temperature=1.3, top_k=7, top_p=0.8),
+    W["tree60_b64_v128256"].with_(B=8, N=33, V=999, dtype="f32", temperature=0.9, top_k=0,
+                                  top_p=1.0),
+    W["chain_g3_v32"].with_(B=500),
+    W["eagle10_v32000"].with_(B=8, temperature=0.0),
+], ids=["c3-reduced", "c4-reduced", "c3-f32", "c4-greedy", "ragged-topk-topp", "f32-plain",
+        "chain", "eagle10-greedy"])
+def test_visited_only_matches_oracle(w):
+    _parity(w, seed=31, flags=binding.SPEC_FLAG_VISITED_ONLY)
+
+
+def test_visited_only_equals_dense_schedule():
+    w = W["tree60_b64_v128256"].with_(B=8, V=40000)
+    inp = gpu_inputs(w, 5)
+    a = run_gpu(w, inp, seed=9)
+    b = run_gpu(w, inp, seed=9, flags=binding.SPEC_FLAG_VISITED_ONLY)
+    for key in ("accept_len", "tokens", "path", "status"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_array_equal(np.isnan(a["alpha"]), np.isnan(b["alpha"]))
+    m = ~np.isnan(a["alpha"])
+    np.testing.assert_allclose(a["alpha"][m], b["alpha"][m], rtol=1e-5, atol=1e-7)
+    # no dense pass: no dense rows read
+    assert b["counters"]["dense_rows"] == 0 and a["counters"]["dense_rows"] > 0

@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--cpu-trees", type=int, default=48,
                     help="tree-steps in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["verify", "commit"], default="verify",
+                    help="commit: time the accepted-path commit on a KV cache instead")
     ap.add_argument("--visited-only", action="store_true",
                     help="the visited-rows-only schedule (no dense pass); reported as its own "
                          "line, not the dense schedule's number")
@@ -509,6 +511,58 @@ def run_ours_lmhead(args, w, world, rank, local, dev):
     return result
 
 
+def run_commit(args):
+    """The accepted-path commit on a KV cache shaped like an 8B model's (32 layers x K/V
+    = 64 planes, 8 heads x 128 x bf16 = 2 KB per position), after verifying the
+    workload's trees: the bytes it moves (read + write) per second."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    seed = shard_seed(args.seed, rank)
+    inp = wl.build_inputs(w, seed=seed, device=dev)
+    out = binding.verify_tree(inp["p"], inp["q"], torch.as_tensor(inp["tokens"], device=dev),
+                              torch.as_tensor(inp["parents"], device=dev), inp["max_depth"],
+                              w.temperature, w.top_k, w.top_p, seed=seed)
+    planes, row_elems, n_pos = 64, 1024, 1024 + w.N
+    cache = torch.zeros((planes, w.B, n_pos, row_elems), dtype=torch.bfloat16, device=dev)
+    prefix = torch.full((w.B,), 1024, dtype=torch.int32, device=dev)
+    acc = out["accept_len"]
+    moved = int(acc.clamp(min=0).sum().item()) * planes * row_elems * 2 * 2
+    for _ in range(args.warmup):
+        binding.commit_accepted_path(cache, prefix, out["path"], acc)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(args.steps):
+        binding.commit_accepted_path(cache, prefix, out["path"], acc)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    peaks, peak_kind = load_peaks()
+    gbs = moved / (ms / 1e3) / 1e9
+    line = {"metric": "accepted-path commit: cache bytes moved (read + write) per second",
+            "value": world * moved / (ms / 1e3), "unit": "B/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "cache": f"{planes} planes x {w.B} sequences x {n_pos} "
+                       f"positions x {row_elems * 2} B", "accepted_nodes": int(acc.clamp(min=0).sum())},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "kernel": "commit_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": moved, "avg_launch_ms": ms},
+            "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, inp, dev, stream):
     """The same metric through the public C-ABI call with host buffers: every step
     copies the inputs host->device from pinned memory, verifies, and copies the
@@ -573,6 +627,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "commit":
+        run_commit(args)
     else:
         run_ours(args)
 

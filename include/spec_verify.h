@@ -311,6 +311,32 @@ int spec_philox_words(uint64_t seed, uint64_t offset, const int32_t* b_idx,
                       const int32_t* node_idx, int32_t n, uint32_t* out_words,
                       spec_stream_t stream);
 
+/*
+ * Accepted-path commit: after a verify step, keep the cache entries of each tree's
+ * accepted path and move them to consecutive positions after the prefix, so the
+ * target and draft caches (and the feature cache) continue the accepted sequence
+ * ("EAGLE close reading", edgeai1.github.io, section 5: after verification both caches
+ * are trimmed to what was accepted).
+ *
+ * cache: device bytes; the entry of position t of sequence b in plane l (a layer's K
+ *   or V, a head, ...) is the row_bytes bytes at
+ *   cache + l * plane_stride + b * batch_stride + t * pos_stride (strides in bytes).
+ * Node n of tree b sits at position prefix_len[b] + n (node 0, the root, is the last
+ *   accepted token); afterwards position prefix_len[b] + k holds node
+ *   accepted_path[b][k] for k = 0 .. accept_len[b]; every other position keeps its bytes.
+ *   Trees with accept_len < 1 are left as they are.
+ * prefix_len [B], accepted_path [B, W], accept_len [B]: device int32 (the verify
+ *   outputs); moves whose source or destination is at or beyond n_pos are skipped.
+ * The cache, strides and row_bytes must be multiples of 16 bytes; row_bytes <=
+ *   pos_stride.  Asynchronous on `stream`; allocates nothing.
+ * Errors: SPEC_ERR_INVALID_ARG, SPEC_ERR_MISALIGNED, SPEC_ERR_TOO_LARGE, SPEC_ERR_CUDA.
+ */
+int spec_commit_accepted_path(void* cache, int32_t B, int32_t n_planes, int32_t n_pos,
+                              int64_t plane_stride, int64_t batch_stride, int64_t pos_stride,
+                              int64_t row_bytes, const int32_t* prefix_len,
+                              const int32_t* accepted_path, const int32_t* accept_len, int32_t W,
+                              spec_stream_t stream);
+
 /* Static description of a return code (never NULL). */
 const char* spec_error_string(int code);
 

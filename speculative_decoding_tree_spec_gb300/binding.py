@@ -96,6 +96,9 @@ def lib():
             L.spec_verify_tree_fused_lmhead_phases.argtypes = (
                 [ctypes.c_uint32] + L.spec_verify_tree_fused_lmhead.argtypes)
             L.spec_verify_tree_fused_lmhead_phases.restype = ctypes.c_int
+            L.spec_commit_accepted_path.argtypes = [P, i32, i32, i32, i64, i64, i64, i64, P, P, P,
+                                                    i32, P]
+            L.spec_commit_accepted_path.restype = ctypes.c_int
             L.spec_filter_rows.argtypes = [P, ctypes.c_int, i32, i32, i64, SamplingParams, P, P]
             L.spec_filter_rows.restype = ctypes.c_int
             L.spec_philox_words.argtypes = [u64, u64, P, P, i32, P, P]
@@ -291,6 +294,28 @@ def verify_tree_fused_lmhead(features: torch.Tensor, weight: torch.Tensor, q,
         out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
                                     "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))
     return out
+
+
+def commit_accepted_path(cache: torch.Tensor, prefix_len: torch.Tensor, accepted_path: torch.Tensor,
+                         accept_len: torch.Tensor, stream=None) -> None:
+    """spec_commit_accepted_path in place on a cache tensor [planes, B, positions, ...]
+    whose trailing dimensions form one row per position (any dtype)."""
+    if cache.dim() < 3:
+        raise ValueError("cache must be [planes, B, positions, ...]")
+    P, B, n_pos = cache.shape[:3]
+    row_bytes = cache[0, 0, 0].numel() * cache.element_size()
+    es = cache.element_size()
+    if cache[0, 0, 0].numel() > 1 and not cache[0, 0, 0].is_contiguous():
+        raise ValueError("each position's row must be contiguous")
+    for t in (prefix_len, accepted_path, accept_len):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError("prefix_len, accepted_path and accept_len must be contiguous int32")
+    rc = lib().spec_commit_accepted_path(
+        cache.data_ptr(), B, P, n_pos, cache.stride(0) * es, cache.stride(1) * es,
+        cache.stride(2) * es, row_bytes, prefix_len.data_ptr(), accepted_path.data_ptr(),
+        accept_len.data_ptr(), accepted_path.shape[1], _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_commit_accepted_path")
 
 
 def verify_tree_host(p_host: torch.Tensor, q_host, tokens_host: torch.Tensor,

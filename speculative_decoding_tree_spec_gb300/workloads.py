@@ -287,3 +287,52 @@ def host_logits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return bf16_bits(t)
     return t.detach().cpu().contiguous().numpy()
+
+
+# ---------------------------------------------------------------------------------------
+# Draft candidates of an EAGLE-2 dynamic tree (EAGLE / EAGLE-2 paper translation,
+# sections 2.3.1-2.3.2).  The sizes follow the method's usual setting: every expanded
+# node gets `children` candidates, `expand_k` nodes of a layer are expanded, `layers`
+# layers in all (10 / 10 / 6 gives 510 candidates; keeping m = 59 of them makes a
+# 60-node draft).  Which nodes are expanded is drawn at random here, not ranked by value:
+# the tree build reads whatever candidate list it is given.
+# ---------------------------------------------------------------------------------------
+@dataclass
+class DraftCandidates:
+    parent: np.ndarray   # [B, n] int32, -1 = child of the root, else an earlier candidate
+    token: np.ndarray    # [B, n] int32
+    prob: np.ndarray     # [B, n] float32 confidences in [0, 1]
+    root: np.ndarray     # [B] int32
+
+
+def make_draft_candidates(B: int, layers: int = 6, expand_k: int = 10, children: int = 10,
+                          seed: int = 0, vocab: int = 128256, levels: int = 0) -> DraftCandidates:
+    """Seeded candidate lists in creation order.  The confidences of one parent's children
+    are a random split of at most 1 listed in descending order (the draft model's top
+    children); levels > 0 rounds every confidence down to a multiple of 1/levels, which
+    makes many values tie."""
+    rng = np.random.default_rng(seed)
+    n = children + (layers - 1) * expand_k * children
+    par = np.empty((B, n), dtype=np.int32)
+    prob = np.empty((B, n), dtype=np.float32)
+    for b in range(B):
+        groups = [-1]
+        start = 0
+        for layer in range(layers):
+            pos = start
+            for g in groups:
+                w = rng.exponential(1.0, size=children + 1)
+                share = np.sort(w[:children] / w.sum())[::-1]
+                par[b, pos:pos + children] = g
+                prob[b, pos:pos + children] = share.astype(np.float32)
+                pos += children
+            layer_nodes = np.arange(start, pos)
+            start = pos
+            if layer + 1 < layers:
+                groups = sorted(rng.choice(layer_nodes, size=min(expand_k, len(layer_nodes)),
+                                           replace=False).tolist())
+    if levels > 0:
+        prob = (np.floor(prob * levels) / levels).astype(np.float32)
+    token = rng.integers(0, vocab, size=(B, n)).astype(np.int32)
+    root = rng.integers(0, vocab, size=B).astype(np.int32)
+    return DraftCandidates(par, token, prob, root)

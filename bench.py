@@ -59,8 +59,9 @@ def parse_args():
     ap.add_argument("--cpu-trees", type=int, default=48,
                     help="tree-steps in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["verify", "commit"], default="verify",
-                    help="commit: time the accepted-path commit on a KV cache instead")
+    ap.add_argument("--op", choices=["verify", "commit", "tree"], default="verify",
+                    help="commit: time the accepted-path commit on a KV cache instead; tree: "
+                         "the EAGLE-2 dynamic draft-tree build (expansion + rerank + mask)")
     ap.add_argument("--visited-only", action="store_true",
                     help="the visited-rows-only schedule (no dense pass); reported as its own "
                          "line, not the dense schedule's number")
@@ -563,6 +564,110 @@ def run_commit(args):
         print(json.dumps(line), flush=True)
 
 
+def run_tree(args):
+    """The EAGLE-2 dynamic draft tree for the workload's batch: the draft model's
+    candidates in the method's usual setting (10 children per expanded node, 10 nodes
+    expanded per layer, 6 layers: 510 candidates), one expansion top-k per layer that
+    feeds the next, then the rerank to the workload's N nodes, flattening and the
+    ancestor mask.  Drafts built per second."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    layers, ek, ch = 6, 10, 10
+    d = wl.make_draft_candidates(w.B, layers=layers, expand_k=ek, children=ch,
+                                 seed=shard_seed(args.seed, rank))
+    par, tok, prob, root = (torch.from_numpy(x).to(dev) for x in (d.parent, d.token, d.prob, d.root))
+    n, m = d.parent.shape[1], w.N - 1
+    bounds = [(0, ch)] + [(ch + i * ek * ch, ch + (i + 1) * ek * ch) for i in range(layers - 2)]
+
+    def step():
+        for lo, hi in bounds:
+            binding.tree_expand_topk(par, prob, lo, hi, ek)
+        return binding.tree_build(par, tok, prob, root, m)
+
+    # the step's launches go through a CUDA graph (six tiny launches: host-bound
+    # otherwise); the e2e figure below is the plain call path with host buffers
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+
+    # end to end: candidates from pinned host memory in, the draft back out, every step
+    host = [torch.from_numpy(x).pin_memory() for x in (d.parent, d.token, d.prob, d.root)]
+    dbuf = [h.to(dev) for h in host]
+
+    def e2e_step():
+        for h, x in zip(host, dbuf):
+            x.copy_(h, non_blocking=True)
+        for lo, hi in bounds:
+            binding.tree_expand_topk(dbuf[0], dbuf[2], lo, hi, ek)
+        out = binding.tree_build(*dbuf, m)
+        return {k: v.to("cpu", non_blocking=True) for k, v in out.items()}
+
+    for _ in range(3):
+        res = e2e_step()
+    torch.cuda.synchronize()
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = sum(v.numel() * v.element_size() for v in res.values())
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.e2e_steps
+    peaks, peak_kind = load_peaks()
+    M = m + 1
+    # per tree: the candidate list read by each expansion (parents + confidences of the
+    # chains it walks, counted once) and by the build (parents, tokens, confidences),
+    # plus the draft written (4 int32 arrays + the mask)
+    bytes_step = w.B * (len(bounds) * n * 8 + n * 12 + M * 16 + M * M)
+    gbs = bytes_step / (ms / 1e3) / 1e9
+    line = {"metric": "EAGLE-2 draft trees built (expand + rerank + flatten + mask) per second",
+            "value": world * w.B / (ms / 1e3), "unit": "trees/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"eagle2_tree_b{w.B}_n{n}_m{m}", "candidates": n,
+                       "draft_nodes": M, "expansions_per_step": len(bounds)},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "kernel": "tree_expand_kernel + tree_build_kernel (whole step)",
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": bytes_step, "avg_launch_ms": ms,
+                         "note": "latency-bound: a few KB per tree, one CTA per tree"},
+            "e2e": {"value": world * w.B / (e2e_ms / 1e3), "unit": "trees/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "timing": "CUDA graph replay of the step; inputs resident, outputs left in HBM",
+            "gpu_launches": args.steps * (len(bounds) + 1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, inp, dev, stream):
     """The same metric through the public C-ABI call with host buffers: every step
     copies the inputs host->device from pinned memory, verifies, and copies the
@@ -629,6 +734,8 @@ def main():
         run_reference(args)
     elif args.op == "commit":
         run_commit(args)
+    elif args.op == "tree":
+        run_tree(args)
     else:
         run_ours(args)
 

@@ -337,6 +337,41 @@ int spec_commit_accepted_path(void* cache, int32_t B, int32_t n_planes, int32_t 
                               const int32_t* accepted_path, const int32_t* accept_len, int32_t W,
                               spec_stream_t stream);
 
+/*
+ * EAGLE-2 dynamic draft tree (EAGLE / EAGLE-2 paper translation, modelers.csdn.net,
+ * sections 2.3.1-2.3.2; "LLM speculative decoding: EAGLE", jingming.pro, 4.2.1).
+ * The draft model's candidates of tree b are given in creation order (layer by layer):
+ * cand_parent [B, n] (the parent candidate, < its own number, or -1 for a child of
+ * the root), cand_token [B, n], cand_prob [B, n] (the draft model's confidence, in
+ * [0, 1]).  A candidate's value is the product of the confidences from the root,
+ * taken root-first in fp32 (v = v_parent * p, v_root = 1).  All arrays are device
+ * arrays; n <= 4096.
+ *
+ * spec_tree_expand_topk: the expansion step -- the k candidates of [layer_begin,
+ *   layer_end) with the largest values (ties to the lower number), into out_idx [B, k]
+ *   (-1 where fewer exist).
+ * spec_tree_build: the reranking and flattening step -- the m candidates with the
+ *   largest values over all layers (a shallower candidate wins a tie, then the lower
+ *   number), flattened after the root breadth-first (by depth, then number):
+ *   out_tokens [B, m+1] (root_token[b] first), out_parent_idx [B, m+1] (-1 for the
+ *   root; the input spec_verify_tree takes), out_position_ids [B, m+1] (depth),
+ *   out_src [B, m+1] (candidate number, -1 for the root), out_mask [B, m+1, m+1]
+ *   (1 where column j is row i or an ancestor of it: the tree attention mask);
+ *   out_status [B] (optional): SPEC_TREE_INVALID for a malformed candidate list (a
+ *   parent not before its child, a confidence outside [0, 1] or NaN, a chain deeper
+ *   than 64), whose outputs are then -1 (mask 0); SPEC_TREE_OK otherwise.
+ *   spec_tree_expand_topk skips malformed candidates.
+ * Errors: SPEC_ERR_INVALID_ARG (sizes, null pointers), SPEC_ERR_CUDA.
+ */
+int spec_tree_expand_topk(const int32_t* cand_parent, const float* cand_prob, int32_t B,
+                          int32_t n, int32_t layer_begin, int32_t layer_end, int32_t k,
+                          int32_t* out_idx, spec_stream_t stream);
+int spec_tree_build(const int32_t* cand_parent, const int32_t* cand_token,
+                    const float* cand_prob, const int32_t* root_token, int32_t B, int32_t n,
+                    int32_t m, int32_t* out_tokens, int32_t* out_parent_idx,
+                    int32_t* out_position_ids, int32_t* out_src, uint8_t* out_mask,
+                    int32_t* out_status, spec_stream_t stream);
+
 /* Static description of a return code (never NULL). */
 const char* spec_error_string(int code);
 

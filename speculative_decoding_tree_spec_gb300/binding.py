@@ -99,6 +99,10 @@ def lib():
             L.spec_commit_accepted_path.argtypes = [P, i32, i32, i32, i64, i64, i64, i64, P, P, P,
                                                     i32, P]
             L.spec_commit_accepted_path.restype = ctypes.c_int
+            L.spec_tree_expand_topk.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
+            L.spec_tree_expand_topk.restype = ctypes.c_int
+            L.spec_tree_build.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P]
+            L.spec_tree_build.restype = ctypes.c_int
             L.spec_filter_rows.argtypes = [P, ctypes.c_int, i32, i32, i64, SamplingParams, P, P]
             L.spec_filter_rows.restype = ctypes.c_int
             L.spec_philox_words.argtypes = [u64, u64, P, P, i32, P, P]
@@ -316,6 +320,44 @@ def commit_accepted_path(cache: torch.Tensor, prefix_len: torch.Tensor, accepted
         accept_len.data_ptr(), accepted_path.shape[1], _stream_ptr(stream))
     if rc != 0:
         raise SpecError(rc, "spec_commit_accepted_path")
+
+
+def tree_expand_topk(cand_parent: torch.Tensor, cand_prob: torch.Tensor, layer_begin: int,
+                     layer_end: int, k: int, stream=None) -> torch.Tensor:
+    """spec_tree_expand_topk: [B, k] int32 candidate numbers to expand next."""
+    B, n = cand_parent.shape
+    out = torch.empty((B, k), dtype=torch.int32, device=cand_parent.device)
+    rc = lib().spec_tree_expand_topk(cand_parent.data_ptr(), cand_prob.data_ptr(), B, n,
+                                     layer_begin, layer_end, k, out.data_ptr(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_tree_expand_topk")
+    return out
+
+
+def tree_build(cand_parent: torch.Tensor, cand_token: torch.Tensor, cand_prob: torch.Tensor,
+               root_token: torch.Tensor, m: int, stream=None) -> dict:
+    """spec_tree_build: the flattened draft (tokens, parent_idx, position_ids, src, mask,
+    status) of every tree."""
+    B, n = cand_parent.shape
+    dev = cand_parent.device
+    for t in (cand_parent, cand_token, root_token):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError("candidate parents, tokens and roots must be contiguous int32")
+    if cand_prob.dtype != torch.float32 or not cand_prob.is_contiguous():
+        raise TypeError("cand_prob must be contiguous float32")
+    M = m + 1
+    out = {k: torch.empty((B, M), dtype=torch.int32, device=dev)
+           for k in ("tokens", "parent_idx", "position_ids", "src")}
+    out["mask"] = torch.empty((B, M, M), dtype=torch.uint8, device=dev)
+    out["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib().spec_tree_build(cand_parent.data_ptr(), cand_token.data_ptr(), cand_prob.data_ptr(),
+                               root_token.data_ptr(), B, n, m, out["tokens"].data_ptr(),
+                               out["parent_idx"].data_ptr(), out["position_ids"].data_ptr(),
+                               out["src"].data_ptr(), out["mask"].data_ptr(),
+                               out["status"].data_ptr(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_tree_build")
+    return out
 
 
 def verify_tree_host(p_host: torch.Tensor, q_host, tokens_host: torch.Tensor,

@@ -143,3 +143,29 @@ def test_philox_validation(L):
     assert L.spec_philox_words(1, 0, FAKE, FAKE, -1, FAKE, None) == -1
     assert L.spec_philox_words(1, 0, None, FAKE, 4, FAKE, None) == -1
     assert L.spec_philox_words(1, 0, FAKE, FAKE, 4, FAKE + 4, None) == -3
+
+
+def test_tree_build_validation(L):
+    f = L.spec_tree_build
+    args = [FAKE] * 4
+    outs = [FAKE] * 7
+    assert f(*args, 0, 10, 5, *outs, None) == 0            # no trees: nothing launched
+    assert f(*args, -1, 10, 5, *outs, None) == -1
+    assert f(*args, 1, 0, 1, *outs, None) == -1            # no candidates
+    assert f(*args, 1, 4097, 5, *outs, None) == -1         # above the candidate limit
+    assert f(*args, 1, 10, 0, *outs, None) == -1           # keeps nothing
+    assert f(*args, 1, 10, 11, *outs, None) == -1          # m > n
+    assert f(*args, 1, 4096, 4096, *outs, None) == -1      # m + 1 nodes above the limit
+    assert f(None, FAKE, FAKE, FAKE, 1, 10, 5, *outs, None) == -1
+    assert f(*args, 1, 10, 5, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == -1
+
+
+def test_tree_expand_validation(L):
+    f = L.spec_tree_expand_topk
+    assert f(FAKE, FAKE, 0, 10, 0, 10, 3, FAKE, None) == 0
+    assert f(FAKE, FAKE, 1, 10, 5, 4, 3, FAKE, None) == -1    # empty-backwards range
+    assert f(FAKE, FAKE, 1, 10, 0, 11, 3, FAKE, None) == -1   # range past n
+    assert f(FAKE, FAKE, 1, 10, -1, 5, 3, FAKE, None) == -1
+    assert f(FAKE, FAKE, 1, 10, 0, 10, 0, FAKE, None) == -1   # k = 0
+    assert f(FAKE, None, 1, 10, 0, 10, 3, FAKE, None) == -1
+    assert f(FAKE, FAKE, 1, 10, 0, 10, 3, None, None) == -1

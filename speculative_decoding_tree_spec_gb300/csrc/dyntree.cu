@@ -16,8 +16,13 @@
 //     candidate number); the parent of each position, its position id (depth), the
 //     candidate it came from, and the attention mask that lets a position see only
 //     its ancestors and itself.
-// One CTA per tree; the orders are bitonic sorts of 64-bit keys built so that a
-// descending sort is (value desc, depth asc, number asc).
+// One CTA per tree.  A candidate's 64-bit key orders (value desc, depth asc, number
+// asc) as an unsigned integer; the rerank is a radix select of the m largest keys
+// (8-bit digits, most significant first, stopping at the first digit whose bin is
+// taken whole), the orders within a list are counts of the keys above (short lists)
+// or bitonic sorts (long ones).
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace svk {
@@ -71,6 +76,84 @@ __device__ void bitonic_desc(uint64_t* keys, int n_pad) {
   }
 }
 
+// Lists up to kRankMax long are ordered by counting (one pass over the list per
+// member, no barriers); longer ones by a bitonic sort.
+constexpr int kRankMax = 1024;
+
+// r[q] = the number of keys[0, cnt) that come before the key of member
+// threadIdx.x + q * blockDim (Desc: larger keys first; else smaller first).  A warp
+// with no member in a round skips it.
+template <int R, bool Desc, typename K>
+__device__ __forceinline__ void count_before(const K* keys, int cnt, int (&r)[R]) {
+  const int warp_base = threadIdx.x & ~31;
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    r[q] = 0;
+    if (warp_base + q * kTreeThreads >= cnt) continue;
+    const int i = threadIdx.x + q * kTreeThreads;
+    const K mine = i < cnt ? keys[i] : K(0);
+    int c = 0;
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) c += Desc ? (keys[j] > mine) : (keys[j] < mine);
+    r[q] = c;
+  }
+}
+
+struct RadixState {
+  unsigned long long prefix;
+  int digit, need, bin, taken;
+};
+
+// The m largest of the distinct keys[0, n), into lst[0, m) in no particular order.
+// Invariant of a pass: every key above `prefix` on the bits in `mask` is taken, and
+// `need` more are to come from the keys equal to it there.
+__device__ void radix_select_top(const uint64_t* keys, int n, int m, int* lst, unsigned* hist,
+                                 RadixState* st) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t prefix = 0ull, mask = 0ull;
+  int need = m;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int d = threadIdx.x; d < 256; d += blockDim.x) hist[d] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds digits 255 - 8l down to 248 - 8l
+      unsigned c[8], sum = 0u;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) { c[t] = hist[255 - 8 * lane - t]; sum += c[t]; }
+      unsigned incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      unsigned above = incl - sum;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (above < (unsigned)need && above + c[t] >= (unsigned)need) {
+          st->digit = 255 - 8 * lane - t;
+          st->need = need - (int)above;
+          st->bin = (int)c[t];
+        }
+        above += c[t];
+      }
+    }
+    __syncthreads();
+    prefix |= (uint64_t)st->digit << shift;
+    mask |= 0xFFull << shift;
+    need = st->need;
+    if (st->bin == need) break;  // the whole bin is taken (the same for every thread)
+  }
+  if (threadIdx.x == 0) st->taken = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    if ((keys[i] & mask) >= prefix) lst[atomicAdd(&st->taken, 1)] = i;
+}
+
 struct TreeBuildJob {
   const int32_t* par;    // [B, n]
   const int32_t* tok;    // [B, n]
@@ -97,6 +180,11 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeBuildJob j
   int* flat_par = depth_of + n;                           // [M]
   int32_t* par = flat_par + M;                            // [n] staged parents
   float* prob = reinterpret_cast<float*>(par + n);        // [n] staged confidences
+  int* bfs = reinterpret_cast<int*>(prob + n);            // [m] kept, breadth-first
+  int* lst = bfs + m;                                     // [m] kept, by value
+  uint32_t* k2 = reinterpret_cast<uint32_t*>(lst + m);    // [m]
+  __shared__ unsigned hist[256];
+  __shared__ RadixState rst;
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -134,24 +222,45 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeBuildJob j
     return;
   }
   // rerank: the m largest keys
-  bitonic_desc(keys, n_pad);
-  // flatten the kept candidates breadth-first: ascending (depth, number) is descending
-  // on its complement
-  // (each entry is rewritten by the one thread that reads it)
-  for (int j = threadIdx.x; j < n_pad; j += blockDim.x) {
-    uint64_t k2 = 0ull;
-    if (j < m) {
-      const int i = 0xFFFFFF - (int)(keys[j] & 0xFFFFFFu);
-      k2 = ((uint64_t)(kMaxDepth - depth_of[i]) << 32) | (uint64_t)(0xFFFFFF - i);
+  radix_select_top(keys, n, m, lst, hist, &rst);
+  __syncthreads();
+  // flatten: breadth-first, i.e. ascending (depth, number)
+  if (m <= kRankMax) {
+    for (int t = threadIdx.x; t < m; t += blockDim.x) {
+      const int i = lst[t];
+      k2[t] = ((uint32_t)depth_of[i] << 24) | (uint32_t)i;
     }
-    keys[j] = k2;
+    __syncthreads();
+    auto place = [&](auto rr) {
+      constexpr int R = decltype(rr)::value;
+      int r[R];
+      count_before<R, false>(k2, m, r);
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int t = threadIdx.x + q * kTreeThreads;
+        if (t < m) bfs[r[q]] = lst[t];
+      }
+    };
+    if (m <= kTreeThreads) place(std::integral_constant<int, 1>());
+    else if (m <= 2 * kTreeThreads) place(std::integral_constant<int, 2>());
+    else place(std::integral_constant<int, 4>());
+  } else {
+    // descending on the complement of (depth, number); the other entries sort last
+    for (int j = threadIdx.x; j < n_pad; j += blockDim.x) {
+      uint64_t key2 = 0ull;
+      if (j < m) {
+        const int i = lst[j];
+        key2 = ((uint64_t)(kMaxDepth - depth_of[i]) << 32) | (uint64_t)(0xFFFFFF - i);
+      }
+      keys[j] = key2;
+    }
+    __syncthreads();
+    bitonic_desc(keys, n_pad);
+    for (int j = threadIdx.x; j < m; j += blockDim.x)
+      bfs[j] = 0xFFFFFF - (int)(keys[j] & 0xFFFFFFu);
   }
   __syncthreads();
-  bitonic_desc(keys, n_pad);
-  for (int j = threadIdx.x; j < m; j += blockDim.x) {
-    const int i = 0xFFFFFF - (int)(keys[j] & 0xFFFFFFu);
-    pos_of[i] = j + 1;
-  }
+  for (int j = threadIdx.x; j < m; j += blockDim.x) pos_of[bfs[j]] = j + 1;
   __syncthreads();
   for (int j = threadIdx.x; j < M; j += blockDim.x) {
     if (j == 0) {
@@ -161,7 +270,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_build_kernel(TreeBuildJob j
       osrc[0] = -1;
       flat_par[0] = -1;
     } else {
-      const int i = 0xFFFFFF - (int)(keys[j - 1] & 0xFFFFFFu);
+      const int i = bfs[j - 1];
       const int p = par[i];
       const int pp = (p < 0) ? 0 : pos_of[p];
       otok[j] = job.tok[(int64_t)b * n + i];
@@ -216,10 +325,31 @@ __global__ void __launch_bounds__(kTreeThreads)
     keys[j] = key;
   }
   __syncthreads();
+  int32_t* out = out_idx + (int64_t)b * k;
+  if (cnt <= kRankMax) {
+    // place = the number of keys above; malformed candidates (key 0) take no place
+    auto place = [&](auto rr) {
+      constexpr int R = decltype(rr)::value;
+      int r[R];
+      count_before<R, true>(keys, cnt, r);
+      int valid = 0;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int j = threadIdx.x + q * kTreeThreads;
+        const bool ok = j < cnt && keys[j] != 0ull;
+        if (ok && r[q] < k) out[r[q]] = lo + j;
+        valid += __syncthreads_count(ok);
+      }
+      for (int j = valid + threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    };
+    if (cnt <= kTreeThreads) place(std::integral_constant<int, 1>());
+    else if (cnt <= 2 * kTreeThreads) place(std::integral_constant<int, 2>());
+    else place(std::integral_constant<int, 4>());
+    return;
+  }
   bitonic_desc(keys, n_pad);
   for (int j = threadIdx.x; j < k; j += blockDim.x)
-    out_idx[(int64_t)b * k + j] =
-        (j < cnt && keys[j] != 0ull) ? 0xFFFFFF - (int)(keys[j] & 0xFFFFFFu) : -1;
+    out[j] = (j < cnt && keys[j] != 0ull) ? 0xFFFFFF - (int)(keys[j] & 0xFFFFFFu) : -1;
 }
 
 }  // namespace
@@ -262,7 +392,7 @@ extern "C" int spec_tree_build(const int32_t* cand_parent, const int32_t* cand_t
     return SPEC_ERR_INVALID_ARG;
   int n_pad = 2;
   while (n_pad < n) n_pad <<= 1;
-  const size_t smem = (size_t)n_pad * sizeof(uint64_t) + (size_t)(4 * n + m + 1) * sizeof(int);
+  const size_t smem = (size_t)n_pad * sizeof(uint64_t) + (size_t)(4 * n + 4 * m + 1) * sizeof(int);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)

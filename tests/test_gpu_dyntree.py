@@ -64,7 +64,8 @@ def _random_forest(B, n, seed, levels=0):
     return wl.DraftCandidates(par, tok, prob, root)
 
 
-@pytest.mark.parametrize("n,m", [(4096, 4095), (4096, 60), (777, 300)])
+@pytest.mark.parametrize("n,m", [(4096, 4095), (4096, 60), (777, 300), (777, 700), (2000, 1024),
+                                 (2000, 1025), (300, 300)])
 def test_build_max_sizes(n, m):
     _check_build(_random_forest(2, n, seed=n + m, levels=16), m)
 
@@ -154,3 +155,18 @@ def test_built_draft_feeds_verify():
     assert res["status"].cpu().tolist() == [0] * 4
     got = res["accept_len"].cpu().tolist()
     assert got == want
+
+
+@pytest.mark.parametrize("levels", [0, 16], ids=["continuous", "tied"])
+def test_expand_long_ranges(levels):
+    """Ranges past one, two and four members per thread, and past the counting limit."""
+    d = _random_forest(3, 4096, seed=77 + levels, levels=levels)
+    par, _, prob, _ = _dev(d)
+    vals = [dyntree.values_and_depths(d.parent[b], d.prob[b])[0] for b in range(3)]
+    for lo, hi in [(0, 256), (100, 400), (1000, 1600), (2000, 3024), (3000, 4096), (0, 4096)]:
+        for k in (7, 300):
+            got = binding.tree_expand_topk(par, prob, lo, hi, k).cpu().numpy()
+            for b in range(3):
+                ref = [lo + i for i in dyntree.expand_topk(vals[b][lo:hi], k)]
+                ref += [-1] * (k - len(ref))
+                assert got[b].tolist() == ref, (lo, hi, k, b)

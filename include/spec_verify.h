@@ -338,6 +338,31 @@ int spec_commit_accepted_path(void* cache, int32_t B, int32_t n_planes, int32_t 
                               spec_stream_t stream);
 
 /*
+ * Per-request sampling parameters: spec_verify_tree_phases with each tree verified
+ * under its own temperature, top-k and top-p (a batch that serves requests with
+ * different sampling settings).  temperature [B] (required), top_k [B] and top_p [B]
+ * (each may be NULL: off) are DEVICE arrays read by the kernels; tree b is verified
+ * exactly as it would be in a spec_verify_tree call with those values, keyed by its
+ * own batch index b for the Philox draws.  A tree with temperature 0 takes the greedy
+ * argmax chain (its draft rows are not read).  The normalisation is the launch's:
+ * top_k <= 0 or >= V is off, top_p >= 1 is off.  A tree whose values are invalid
+ * (temperature negative, infinite or NaN; top_p <= 0 or NaN; top_k < 0) gets status
+ * SPEC_TREE_INVALID.  logits_q is required.  flags are the launch's SPEC_FLAG_* bits;
+ * phases, layouts, workspace, outputs and return codes as spec_verify_tree_phases.
+ */
+int spec_verify_tree_per_request(uint32_t phases, const void* logits_p, const void* logits_q,
+                                 spec_dtype dtype, int32_t B, int32_t N, int32_t V,
+                                 int64_t row_pitch, int64_t batch_stride,
+                                 const int32_t* draft_tokens, const int32_t* parent_idx,
+                                 int32_t max_depth, const float* temperature,
+                                 const int32_t* top_k, const float* top_p, uint32_t flags,
+                                 uint64_t rng_seed, uint64_t rng_offset, int32_t* out_accept_len,
+                                 int32_t* out_tokens, int32_t* out_accepted_path,
+                                 float* out_alpha, int32_t* out_status,
+                                 spec_verify_counters* out_counters, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * EAGLE-2 dynamic draft tree (EAGLE / EAGLE-2 paper translation, modelers.csdn.net,
  * sections 2.3.1-2.3.2; "LLM speculative decoding: EAGLE", jingming.pro, 4.2.1).
  * The draft model's candidates of tree b are given in creation order (layer by layer):

@@ -195,3 +195,25 @@ def verify_tree(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
         _ptr(out["tokens"]), _ptr(out["path"]), _ptr(out["alpha"]), _ptr(out["status"]),
         _ptr(out["near"]), _ptr(out.get("final_dist")), int(nthreads))
     return out
+
+
+def verify_tree_per_request(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
+                            temperature, top_k, top_p, seed: int, offset: int = 0):
+    """Per-request sampling parameters (one batch serving requests with different
+    settings).  Reading taken here: tree b is verified exactly as a batch of one under
+    its own temperature[b], top_k[b], top_p[b], drawing its uniforms as batch index b;
+    a tree whose values are invalid (temperature negative or not finite, top_p <= 0 or
+    NaN, top_k < 0) gets status 2 (invalid) and accept_len -1."""
+    tokens = np.asarray(draft_tokens)
+    B = tokens.shape[0]
+    outs = []
+    for b in range(B):
+        T, k, p = float(temperature[b]), int(top_k[b]), float(top_p[b])
+        if not (np.isfinite(T) and T >= 0.0) or not (p > 0.0) or k < 0:
+            outs.append(None)
+            continue
+        outs.append(verify_tree(logits_p[b:b + 1], logits_q[b:b + 1], tokens[b:b + 1],
+                                np.asarray(parent_idx)[b:b + 1], max_depth, T, k, p, seed,
+                                offset, batch_index=b))
+    return outs
+

@@ -99,6 +99,11 @@ def lib():
             L.spec_commit_accepted_path.argtypes = [P, i32, i32, i32, i64, i64, i64, i64, P, P, P,
                                                     i32, P]
             L.spec_commit_accepted_path.restype = ctypes.c_int
+            L.spec_verify_tree_per_request.argtypes = [
+                ctypes.c_uint32, P, P, ctypes.c_int, i32, i32, i32, ctypes.c_int64, ctypes.c_int64,
+                P, P, i32, P, P, P, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_uint64,
+                P, P, P, P, P, P, P, ctypes.c_size_t, P]
+            L.spec_verify_tree_per_request.restype = ctypes.c_int
             L.spec_tree_expand_topk.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
             L.spec_tree_expand_topk.restype = ctypes.c_int
             L.spec_tree_build.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P]
@@ -199,6 +204,61 @@ def verify_tree(p: torch.Tensor, q, draft_tokens: torch.Tensor, parent_idx: torc
         workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     if rc != 0:
         raise SpecError(rc, "spec_verify_tree")
+    if counters is not None:
+        c = counters.cpu().numpy().view("uint64")
+        out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",
+                                    "final_draws", "fallback_rows"], [int(x) for x in c[:6]]))
+    return out
+
+
+def verify_tree_per_request(p: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Tensor,
+                            parent_idx: torch.Tensor, max_depth: int, temperature: torch.Tensor,
+                            top_k=None, top_p=None, seed: int = 0, offset: int = 0,
+                            flags: int = 0, *, want_alpha: bool = True,
+                            want_counters: bool = False, workspace=None, stream=None,
+                            phases: int = SPEC_PHASE_ALL):
+    """spec_verify_tree_per_request: tree b verified under temperature[b], top_k[b],
+    top_p[b] (device tensors [B]: float32, int32, float32; top_k / top_p may be None).
+    Returns the same dict as verify_tree."""
+    B, N = draft_tokens.shape
+    V = p.shape[-1]
+    dev = p.device
+    if draft_tokens.dtype != torch.int32 or parent_idx.dtype != torch.int32:
+        raise TypeError("draft_tokens and parent_idx must be int32")
+    if q is None or q.dtype != p.dtype:
+        raise TypeError("p and q logits must share a dtype")
+    pitch, bstride = _row_layout(p, B, N, V, False)
+    if _row_layout(q, B, N, V, False) != (pitch, bstride):
+        raise ValueError("p and q must share one layout")
+    for t, dt in ((temperature, torch.float32), (top_k, torch.int32), (top_p, torch.float32)):
+        if t is not None and (t.dtype != dt or t.shape != (B,) or t.device != dev
+                              or not t.is_contiguous()):
+            raise TypeError("per-request arrays must be contiguous [B] tensors on the logits' device")
+    W = max_depth + 1
+    out = {
+        "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+        "tokens": torch.empty((B, W), dtype=torch.int32, device=dev),
+        "path": torch.empty((B, W), dtype=torch.int32, device=dev),
+        "status": torch.empty(B, dtype=torch.int32, device=dev),
+    }
+    if want_alpha:
+        out["alpha"] = torch.empty((B, N), dtype=torch.float32, device=dev)
+    dt = _dtype_code(p)
+    ws_bytes = int(lib().spec_verify_workspace_size(B, N, V, dt))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    counters = torch.zeros(8, dtype=torch.int64, device=dev) if want_counters else None
+    rc = lib().spec_verify_tree_per_request(
+        int(phases), p.data_ptr(), q.data_ptr(), dt, B, N, V, pitch, bstride,
+        draft_tokens.data_ptr(), parent_idx.data_ptr(), int(max_depth), temperature.data_ptr(),
+        None if top_k is None else top_k.data_ptr(), None if top_p is None else top_p.data_ptr(),
+        int(flags), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+        out["accept_len"].data_ptr(), out["tokens"].data_ptr(), out["path"].data_ptr(),
+        out["alpha"].data_ptr() if "alpha" in out else None, out["status"].data_ptr(),
+        None if counters is None else counters.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_verify_tree_per_request")
     if counters is not None:
         c = counters.cpu().numpy().view("uint64")
         out["counters"] = dict(zip(["dense_rows", "dense_bytes", "walk_bytes", "residual_passes",

@@ -69,17 +69,18 @@ extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t N, int32_t V, sp
   return ws_layout(B > 0 ? B : 1, N).total;
 }
 
-extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
-                                       const void* logits_q, spec_dtype dtype, int32_t B,
-                                       int32_t N, int32_t V, int64_t row_pitch,
-                                       int64_t batch_stride, const int32_t* draft_tokens,
-                                       const int32_t* parent_idx, int32_t max_depth,
-                                       spec_sampling_params params, uint64_t rng_seed,
-                                       uint64_t rng_offset, int32_t* out_accept_len,
-                                       int32_t* out_tokens, int32_t* out_accepted_path,
-                                       float* out_alpha, int32_t* out_status,
-                                       spec_verify_counters* out_counters, void* workspace,
-                                       size_t workspace_bytes, spec_stream_t stream) {
+namespace {
+
+// One verify call; req_* are the per-request arrays (null: the launch's params).
+int verify_impl(uint32_t phases, const void* logits_p, const void* logits_q, spec_dtype dtype,
+                int32_t B, int32_t N, int32_t V, int64_t row_pitch, int64_t batch_stride,
+                const int32_t* draft_tokens, const int32_t* parent_idx, int32_t max_depth,
+                spec_sampling_params params, const float* req_temperature,
+                const int32_t* req_top_k, const float* req_top_p, uint64_t rng_seed,
+                uint64_t rng_offset, int32_t* out_accept_len, int32_t* out_tokens,
+                int32_t* out_accepted_path, float* out_alpha, int32_t* out_status,
+                spec_verify_counters* out_counters, void* workspace, size_t workspace_bytes,
+                spec_stream_t stream) {
   if (phases == 0 || (phases & ~SPEC_PHASE_ALL)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (B < 0 || N < 1 || V < 1 || max_depth < 0) return SPEC_ERR_INVALID_ARG;
@@ -87,7 +88,8 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
     return SPEC_ERR_TOO_LARGE;
   int rc = check_params(params);
   if (rc != SPEC_OK) return rc;
-  const bool greedy = params.temperature == 0.0f;
+  const bool per_request = req_temperature != nullptr;
+  const bool greedy = !per_request && params.temperature == 0.0f;
   if (!logits_p || (!greedy && !logits_q) || !draft_tokens || !parent_idx || !out_accept_len ||
       !out_tokens || !out_accepted_path || !workspace)
     return SPEC_ERR_INVALID_ARG;
@@ -129,6 +131,12 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   tj.delta_z = kWindowNats * params.temperature;
   tj.exact = (params.flags & SPEC_FLAG_EXACT_SELECT) ? 1 : 0;
   tj.visited_only = (params.flags & SPEC_FLAG_VISITED_ONLY) ? 1 : 0;
+  if (per_request) {
+    tj.req_temperature = req_temperature;
+    tj.req_top_k = req_top_k;
+    tj.req_top_p = req_top_p;
+    tj.trunc = 1;  // any tree may cut: the walk reserves the cut's buffers
+  }
   tj.seed = rng_seed;
   tj.offset = rng_offset;
   tj.out_accept_len = out_accept_len;
@@ -159,6 +167,7 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
   rj.stats_p = stats_p;
   rj.stats_q = stats_q;
   rj.counters = tj.counters;
+  rj.req_temperature = req_temperature;
   const int virtual_rows = B * N * (greedy ? 1 : 2);
   // the visited-rows-only schedule has no dense pass
   if ((phases & SPEC_PHASE_ROWS) && !tj.visited_only &&
@@ -173,6 +182,42 @@ extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
       return SPEC_ERR_CUDA;
   }
   return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_verify_tree_phases(uint32_t phases, const void* logits_p,
+                                       const void* logits_q, spec_dtype dtype, int32_t B,
+                                       int32_t N, int32_t V, int64_t row_pitch,
+                                       int64_t batch_stride, const int32_t* draft_tokens,
+                                       const int32_t* parent_idx, int32_t max_depth,
+                                       spec_sampling_params params, uint64_t rng_seed,
+                                       uint64_t rng_offset, int32_t* out_accept_len,
+                                       int32_t* out_tokens, int32_t* out_accepted_path,
+                                       float* out_alpha, int32_t* out_status,
+                                       spec_verify_counters* out_counters, void* workspace,
+                                       size_t workspace_bytes, spec_stream_t stream) {
+  return verify_impl(phases, logits_p, logits_q, dtype, B, N, V, row_pitch, batch_stride,
+                     draft_tokens, parent_idx, max_depth, params, nullptr, nullptr, nullptr,
+                     rng_seed, rng_offset, out_accept_len, out_tokens, out_accepted_path,
+                     out_alpha, out_status, out_counters, workspace, workspace_bytes, stream);
+}
+
+extern "C" int spec_verify_tree_per_request(
+    uint32_t phases, const void* logits_p, const void* logits_q, spec_dtype dtype, int32_t B,
+    int32_t N, int32_t V, int64_t row_pitch, int64_t batch_stride, const int32_t* draft_tokens,
+    const int32_t* parent_idx, int32_t max_depth, const float* temperature, const int32_t* top_k,
+    const float* top_p, uint32_t flags, uint64_t rng_seed, uint64_t rng_offset,
+    int32_t* out_accept_len, int32_t* out_tokens, int32_t* out_accepted_path, float* out_alpha,
+    int32_t* out_status, spec_verify_counters* out_counters, void* workspace,
+    size_t workspace_bytes, spec_stream_t stream) {
+  if (!temperature) return SPEC_ERR_INVALID_ARG;
+  // the launch-wide values only select the sampling row pass; each tree reads its own
+  spec_sampling_params prm{1.0f, 0, 1.0f, flags};
+  return verify_impl(phases, logits_p, logits_q, dtype, B, N, V, row_pitch, batch_stride,
+                     draft_tokens, parent_idx, max_depth, prm, temperature, top_k, top_p,
+                     rng_seed, rng_offset, out_accept_len, out_tokens, out_accepted_path,
+                     out_alpha, out_status, out_counters, workspace, workspace_bytes, stream);
 }
 
 extern "C" int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtype,

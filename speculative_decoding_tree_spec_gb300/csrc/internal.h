@@ -71,8 +71,17 @@ struct RowJob {
   int32_t top_k;  // 0: off
   float top_p;    // >= 1: off
   uint32_t flags;
+  const float* req_temperature;  // [B] per-tree temperatures (kRowsTree), or null
   uint64_t wait_limit_ns;        // bound of every device-side wait
   unsigned long long* counters;  // spec_verify_counters as an array of 8 u64, or null
+};
+
+// The sampling parameters one tree is verified under (the launch's, or the tree's own
+// when per-request arrays are given): c = log2(e) / T, delta_z = the candidate window
+// below the row maximum in logit units, trunc = a top-k / top-p cut is needed.
+struct Samp {
+  float temperature, c, delta_z, top_p;
+  int32_t top_k, trunc;
 };
 
 struct TreeJob {
@@ -95,6 +104,11 @@ struct TreeJob {
   float delta_z;      // candidate window below the row maximum (logit units)
   int32_t exact;      // always take the full-row exact selection
   int32_t visited_only;  // no dense pass: the walk computes the statistics of the rows it visits
+  // per-request sampling parameters, [B] each (null: the launch's values above);
+  // trunc is then 1 (a tree may cut) and each tree reads its own
+  const float* req_temperature;
+  const int32_t* req_top_k;
+  const float* req_top_p;
   uint64_t seed, offset;
   int32_t* out_accept_len;
   int32_t* out_tokens;

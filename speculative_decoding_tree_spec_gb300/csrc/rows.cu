@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
   const int full_units = V / E;
   const int per_iter = NT * U;
   const int niter = (nunits + per_iter - 1) / per_iter;
-  const float c = job.c;
+  const float c_launch = job.c;
   const int BN = job.B * job.N;
   const int total = (job.mode == kRowsList) ? job.R : (job.with_q ? 2 * BN : BN);
   const bool topk_on = job.top_k > 0 && job.top_k < V;
@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
         const bool is_q = v >= BN;
         const int r = is_q ? v - BN : v;
         const int b = r / job.N, n = r - b * job.N;
+        if (is_q && job.req_temperature && !(job.req_temperature[b] > 0.0f)) continue;
         if (is_q) {
           int has_child = 0;
           for (int ch = n + 1 + lane; ch < job.N; ch += 32)
@@ -342,6 +343,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
   for (int v = job.first_row + (int)blockIdx.x; v < total; v += gridDim.x) {
     const void* row;
     spec_row_stats* out;
+    float c = c_launch;
     if (job.mode == kRowsList) {
       row = row_ptr(job.base_p, (int64_t)v * job.row_pitch, Elt<T>::kBytes);
       out = job.stats_p + v;
@@ -349,6 +351,14 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
       const bool is_q = v >= BN;
       const int r = is_q ? v - BN : v;
       const int b = r / job.N, n = r - b * job.N;
+      if (job.req_temperature) {
+        // the tree's own temperature; a greedy tree (or one with an invalid
+        // temperature, which the walk reports) needs only its target rows' argmax
+        const float temp = job.req_temperature[b];
+        const bool sampled = temp > 0.0f && temp <= 3.402823466e38f;
+        if (is_q && !(temp > 0.0f)) continue;
+        c = sampled ? (float)(1.4426950408889634 / (double)temp) : 1.0f;
+      }
       if (is_q) {
         // the draft row of node n is read only if some node has n as its parent
         // (every warp decides for itself, identically)

@@ -452,6 +452,7 @@ struct CShared {
   double wtot[CW];
   double target;
   int accept, status, target_warp, final_tok;
+  Samp smp;  // the tree's sampling parameters
   unsigned err;            // rank 0: timeouts reported by any CTA of the cluster
   float inv_sp, inv_sq;
   unsigned ncand[2];       // window candidates of this CTA's slice, per row
@@ -806,9 +807,9 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
 // n_pad with zeros), or false when the window cannot decide it.  Same rule as the
 // dense row pass's sorted window.
 __device__ bool window_cut(const uint64_t* keys, unsigned n, unsigned n_pad, float m, float c,
-                           double s_all, const TreeJob& job, CShared& sh, RowCut& out) {
-  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
-  const unsigned K = topk_on ? (unsigned)job.top_k : n;
+                           double s_all, const Samp& smp, CShared& sh, RowCut& out) {
+  const bool topk_on = smp.top_k > 0, topp_on = smp.top_p < 1.0f;
+  const unsigned K = topk_on ? (unsigned)smp.top_k : n;
   const int lane = threadIdx.x & 31;
   const unsigned lo = threadIdx.x * (unsigned)kSortPer;
   if (threadIdx.x == 0) sh.first = INT_MAX;
@@ -834,7 +835,7 @@ __device__ bool window_cut(const uint64_t* keys, unsigned n, unsigned n_pad, flo
     }
     __syncthreads();
     const unsigned long long tau = (unsigned long long)ceil(
-        (double)job.top_p * (topk_on ? (double)sh.massk : s_all * 4398046511104.0));
+        (double)smp.top_p * (topk_on ? (double)sh.massk : s_all * 4398046511104.0));
     int fj = INT_MAX;
 #pragma unroll
     for (int t = 0; t < kSortPer; ++t) {
@@ -944,19 +945,20 @@ struct ClusterReduce {
 template <typename T>
 __device__ bool cluster_exact_cut(const TreeJob& job, const void* row, const spec_row_stats& s,
                                   int ua, int ub, CShared& sh, int C, uint32_t rank,
-                                  uint32_t& n_ex, float c, RowCut& out) {
-  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
+                                  uint32_t& n_ex, const Samp& smp, RowCut& out) {
+  const float c = smp.c;
+  const bool topk_on = smp.top_k > 0, topp_on = smp.top_p < 1.0f;
   const int V = job.V;
   ClusterReduce red{&sh, C, rank, &n_ex, true};
   SelOut rk{};
   const Eligible all{false, 0u, 0};
   if (topk_on)
-    rk = exact_select<T, BSync>(row, V, s.m, c, false, (unsigned)job.top_k, 0ull, all, sh.sel,
+    rk = exact_select<T, BSync>(row, V, s.m, c, false, (unsigned)smp.top_k, 0ull, all, sh.sel,
                                 ua, ub, red);
   if (topp_on) {
     const Eligible in_k{topk_on, rk.key, rk.idx};
     const unsigned long long tau = (unsigned long long)ceil(
-        (double)job.top_p * (topk_on ? (double)rk.mass_kept : s.s_f * 4398046511104.0));
+        (double)smp.top_p * (topk_on ? (double)rk.mass_kept : s.s_f * 4398046511104.0));
     const SelOut rp = exact_select<T, BSync>(row, V, s.m, c, true, 0u, tau, in_k, sh.sel, ua,
                                              ub, red);
     out.key = rp.key; out.idx = rp.idx; out.kept = rp.kept; out.mass = rp.mass_kept;
@@ -976,12 +978,13 @@ template <typename T>
 __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const void* qrow,
                                    bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
                                    int ub, uint64_t* cand, uint64_t* sortb, CShared& sh, int C,
-                                   uint32_t rank, uint32_t& n_ex, float c) {
+                                   uint32_t rank, uint32_t& n_ex, const Samp& smp) {
+  const float c = smp.c;
   const int V = job.V;
   const int nrows = with_q ? 2 : 1;
   spec_row_stats* st[2] = {&sp, &sq};
   const void* const rows[2] = {prow, qrow};
-  const float thr[2] = {sp.m - job.delta_z, sq.m - job.delta_z};
+  const float thr[2] = {sp.m - smp.delta_z, sq.m - smp.delta_z};
   uint64_t* const cl[2] = {cand, cand + kCandCTA};
   unsigned* const no_hist[2] = {nullptr, nullptr};
   const uint32_t no_k16[2] = {0u, 0u};
@@ -1001,9 +1004,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
       over |= cnt[r][q] > (unsigned)kCandCTA;
       total[r] += min(cnt[r][q], (unsigned)kCandCTA);
     }
-    const bool topk_on = job.top_k > 0;
+    const bool topk_on = smp.top_k > 0;
     fast[r] = !job.exact && !over && total[r] >= 1u && total[r] <= (unsigned)kSortW &&
-              (!topk_on || total[r] >= (unsigned)job.top_k);
+              (!topk_on || total[r] >= (unsigned)smp.top_k);
     while (n_pad[r] < total[r]) n_pad[r] <<= 1;
   }
   // gather every CTA's candidates (remote shared memory) into the sort buffers
@@ -1042,9 +1045,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
   for (int r = 0; r < nrows; ++r) {
     spec_row_stats& s = *st[r];
     RowCut rc{};
-    bool ok = fast[r] && window_cut(sortb + r * kSortW, total[r], n_pad[r], s.m, c, s.s_f, job,
+    bool ok = fast[r] && window_cut(sortb + r * kSortW, total[r], n_pad[r], s.m, c, s.s_f, smp,
                                     sh, rc);
-    if (!ok && !cluster_exact_cut<T>(job, rows[r], s, ua, ub, sh, C, rank, n_ex, c, rc))
+    if (!ok && !cluster_exact_cut<T>(job, rows[r], s, ua, ub, sh, C, rank, n_ex, smp, rc))
       return false;
     set_cut(s, rc);
   }
@@ -1058,10 +1061,10 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
 // Results in sh.sc_*[r]; sh.sc_ok[r] = 0 when the window cannot decide the cut.
 __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin, int nb,
                                  uint32_t K16m, float m, float c, double s_all,
-                                 const TreeJob& job, CShared& sh, int r) {
+                                 const Samp& smp, CShared& sh, int r) {
   const int lane = threadIdx.x & 31;
-  const bool topk_on = job.top_k > 0, topp_on = job.top_p < 1.0f;
-  const unsigned K = topk_on ? (unsigned)job.top_k : 0u;
+  const bool topk_on = smp.top_k > 0, topp_on = smp.top_p < 1.0f;
+  const unsigned K = topk_on ? (unsigned)smp.top_k : 0u;
   const int Cb = (nb + 31) / 32;
   const int b_lo = min(nb, lane * Cb), b_hi = min(nb, b_lo + Cb);
   unsigned lc = 0;
@@ -1120,7 +1123,7 @@ __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin,
   }
   if (ok && topp_on) {
     const unsigned long long tau = (unsigned long long)ceil(
-        (double)job.top_p * (topk_on ? (double)s_k : s_all * 4398046511104.0));
+        (double)smp.top_p * (topk_on ? (double)s_k : s_all * 4398046511104.0));
     int hitbin = INT_MAX;
     unsigned long long rw = base_w;
     for (int bin = b_lo; bin < b_hi && bin <= b_k; ++bin) {
@@ -1170,7 +1173,8 @@ __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin,
 __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const void* qrow,
                                  bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
                                  int ub, unsigned char* smem, CShared& sh, int C, uint32_t rank,
-                                 uint32_t& n_ex, float c) {
+                                 uint32_t& n_ex, const Samp& smp) {
+  const float c = smp.c;
   const int V = job.V;
   const int nrows = with_q ? 2 : 1;
   spec_row_stats* st[2] = {&sp, &sq};
@@ -1189,7 +1193,7 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   bool fits[2];
   unsigned* hp[2] = {nullptr, nullptr};
   for (int r = 0; r < 2; ++r) {
-    thr[r] = st[r]->m - job.delta_z;
+    thr[r] = st[r]->m - smp.delta_z;
     k16m[r] = order_key(st[r]->m) >> 16;
     uint32_t k16t = order_key(thr[r]) >> 16;  // lowest key the window can hold
     if (k16m[r] - k16t >= (uint32_t)kWalkBins) {
@@ -1229,7 +1233,7 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   if (warp < nrows) {
     if (win[warp])
       bf16_window_scan(merged[warp], wbin[warp], nb[warp], k16m[warp], st[warp]->m, c,
-                       st[warp]->s_f, job, sh, warp);
+                       st[warp]->s_f, smp, sh, warp);
     else if ((threadIdx.x & 31) == 0)
       sh.sc_ok[warp] = 0;
   }
@@ -1359,7 +1363,7 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   for (int r = 0; r < nrows; ++r) {
     if (ok[r]) continue;
     RowCut rc;
-    if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, c, rc))
+    if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, smp, rc))
       return false;
     set_cut(*st[r], rc);
   }
@@ -1496,16 +1500,16 @@ template <typename T>
 __device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qrow, bool with_q,
                             spec_row_stats& sp, spec_row_stats& sq, int ua, int ub,
                             unsigned char* smem, uint32_t n_visit, CShared& sh, int C,
-                            uint32_t rank, uint32_t& n_ex, float c) {
+                            uint32_t rank, uint32_t& n_ex, const Samp& smp) {
   if constexpr (sizeof(T) == 2) {
-    return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, c);
+    return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, smp);
   } else {
     // candidate lists alternate between two sets from node to node (they are read
     // by the other CTAs); then the two sort buffers
     uint64_t* cand = reinterpret_cast<uint64_t*>(smem) + (size_t)(n_visit & 1) * 2 * kCandCTA;
     uint64_t* sortb = reinterpret_cast<uint64_t*>(smem) + 4 * kCandCTA;
     return cluster_cut_sorted<T>(job, prow, qrow, with_q, sp, sq, ua, ub, cand, sortb, sh, C,
-                                 rank, n_ex, c);
+                                 rank, n_ex, smp);
   }
 }
 
@@ -1521,6 +1525,33 @@ constexpr size_t cut_smem_bytes() {
 // ---------------------------------------------------------------------------
 // Sampling walk: one cluster of C CTAs per tree.
 // ---------------------------------------------------------------------------
+// The sampling parameters of tree b: the launch's, or the tree's own from the
+// per-request arrays (the same normalisation as the host applies to the launch's:
+// top_k >= V or 0 is off, top_p >= 1 is off).  Invalid values (a temperature that is
+// negative, infinite or NaN, top_p <= 0 or NaN, top_k < 0) set `status` to
+// SPEC_TREE_INVALID.
+__device__ Samp tree_samp(const TreeJob& job, int b, int& status) {
+  Samp s{job.temperature, job.c, job.delta_z, job.top_p, job.top_k, job.trunc};
+  if (!job.req_temperature) return s;
+  const float T = job.req_temperature[b];
+  const int k = job.req_top_k ? job.req_top_k[b] : 0;
+  const float p = job.req_top_p ? job.req_top_p[b] : 1.0f;
+  if (!(T >= 0.0f && T <= 3.402823466e38f) || !(p > 0.0f) || k < 0) {
+    status = SPEC_TREE_INVALID;
+    s.temperature = 1.0f;
+    s.c = 1.0f;
+    s.trunc = 0;
+    return s;
+  }
+  s.temperature = T;
+  s.c = T > 0.0f ? (float)(1.4426950408889634 / (double)T) : 0.0f;
+  s.delta_z = kWindowNats * T;
+  s.top_k = (k > 0 && k < job.V) ? k : 0;
+  s.top_p = p >= 1.0f ? 1.0f : p;
+  s.trunc = (T > 0.0f && (s.top_k > 0 || s.top_p < 1.0f)) ? 1 : 0;
+  return s;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJob job, int C, int max_steps) {
   __shared__ CShared sh;
@@ -1538,8 +1569,13 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   // the top-k / top-p cut's buffers (16-byte aligned)
   unsigned char* cut_smem = reinterpret_cast<unsigned char*>(
       reinterpret_cast<uintptr_t>(steps + CW * max_steps + 3) & ~(uintptr_t)15);
-  const double Td = (double)job.temperature;
-  const float c = job.c;
+  int status = SPEC_TREE_OK;
+  {
+    const Samp s0 = tree_samp(job, b, status);
+    if (threadIdx.x == 0) sh.smp = s0;
+  }
+  // read from shared memory where used (kept out of the registers)
+  const Samp& smp = sh.smp;
   const bool lead = (rank == 0);
 
   if (threadIdx.x == 0) {
@@ -1549,8 +1585,13 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     fence_barrier_init();
   }
   cluster_sync_all();
+  const double Td = (double)smp.temperature;
+  const float c = smp.c;
 
-  int status = load_tree(job, b, par, tok, cs, cl, lead, &sh.status);
+  {
+    const int st = load_tree(job, b, par, tok, cs, cl, lead, &sh.status);
+    if (status == SPEC_TREE_OK) status = st;
+  }
   const int nunits = (V + E - 1) / E;
   const int ua = (int)((int64_t)nunits * rank / C), ub = (int)((int64_t)nunits * (rank + 1) / C);
   int32_t* out_tok = job.out_tokens + (int64_t)b * W;
@@ -1560,7 +1601,38 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   bool timed_out = false;
   int u = 0, n_acc = 0, final_tok = -1, owner = -1;
 
-  while (status == SPEC_TREE_OK) {
+  // a greedy tree of a per-request batch: the target's argmax chain
+  while (status == SPEC_TREE_OK && smp.temperature == 0.0f) {
+    const void* prow = row_at(job.base_p, job, b, u, Elt<T>::kBytes);
+    spec_row_stats sp, sq;
+    if (job.visited_only) {
+      if (!cluster_row_stats<T>(job, prow, prow, false, sp, sq, ua, ub, sh, C, rank, n_ex, 1.0f)) {
+        timed_out = true;
+        status = SPEC_ROW_TIMEOUT;
+        break;
+      }
+    } else {
+      sp = job.stats_p[(int64_t)b * N + u];
+    }
+    if (sp.status != SPEC_TREE_OK) { status = sp.status; break; }
+    int next = -1;
+    for (int i = cs[u]; i < cs[u + 1]; ++i) {
+      const int ch = cl[i];
+      const bool hit = tok[ch] == sp.argmax;
+      if (lead && threadIdx.x == 0 && job.out_alpha)
+        job.out_alpha[(int64_t)b * N + ch] = hit ? 1.f : 0.f;
+      if (hit) { next = ch; break; }
+    }
+    if (next < 0) { final_tok = sp.argmax; break; }
+    if (lead && threadIdx.x == 0) {
+      out_tok[n_acc] = tok[next];
+      out_path[n_acc + 1] = next;
+    }
+    ++n_acc;
+    u = next;
+  }
+
+  while (status == SPEC_TREE_OK && smp.temperature != 0.0f) {
     const int c0 = cs[u], c1 = cs[u + 1];
     const void* prow = row_at(job.base_p, job, b, u, Elt<T>::kBytes);
     const void* qrow = row_at(job.base_q, job, b, u, Elt<T>::kBytes);
@@ -1591,10 +1663,10 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       sh.kid_k[r][i] = order_key(z);
       if (r == 0) sh.kid_u[i] = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
     }
-    if (job.trunc) {
+    if (smp.trunc) {
       // cut the visited rows
       if (!cluster_cut<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, cut_smem, n_visit++, sh, C,
-                          rank, n_ex, c)) {
+                          rank, n_ex, smp)) {
         timed_out = true;
         status = SPEC_ROW_TIMEOUT;
         break;

@@ -169,3 +169,13 @@ def test_tree_expand_validation(L):
     assert f(FAKE, FAKE, 1, 10, 0, 10, 0, FAKE, None) == -1   # k = 0
     assert f(FAKE, None, 1, 10, 0, 10, 3, FAKE, None) == -1
     assert f(FAKE, FAKE, 1, 10, 0, 10, 3, None, None) == -1
+
+
+def test_per_request_validation(L):
+    f = L.spec_verify_tree_per_request
+    args = lambda T=FAKE, q=FAKE, B=2: (7, FAKE, q, 1, B, 4, 1000, 1000, 4000, FAKE, FAKE, 3, T,
+                                        None, None, 0, 0, 0, FAKE, FAKE, FAKE, None, None, None,
+                                        FAKE, 1 << 20, None)
+    assert f(*args(B=0)) == 0                     # no trees: nothing launched
+    assert f(*args(T=None)) == -1                 # the temperatures are required
+    assert f(*args(q=None)) == -1                 # the draft logits are required

@@ -59,9 +59,10 @@ def parse_args():
     ap.add_argument("--cpu-trees", type=int, default=48,
                     help="tree-steps in the oracle sample of the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["verify", "commit", "tree"], default="verify",
+    ap.add_argument("--op", choices=["verify", "commit", "tree", "draft"], default="verify",
                     help="commit: time the accepted-path commit on a KV cache instead; tree: "
-                         "the EAGLE-2 dynamic draft-tree build (expansion + rerank + mask)")
+                         "the EAGLE-2 dynamic draft-tree build (expansion + rerank + mask); "
+                         "draft: the draft-side top-k drafting of the expanded nodes' rows")
     ap.add_argument("--visited-only", action="store_true",
                     help="the visited-rows-only schedule (no dense pass); reported as its own "
                          "line, not the dense schedule's number")
@@ -668,6 +669,80 @@ def run_tree(args):
         print(json.dumps(line), flush=True)
 
 
+def run_draft(args):
+    """Draft-side top-k drafting: the rows of the nodes one EAGLE-2 layer expands (the
+    workload's batch x 10 expanded nodes) of draft logits over the workload's vocabulary
+    (bf16, N(0, 3^2)), the 10 children and confidences of each at T = 1.  Rows per second
+    and the HBM roofline of the one kernel."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    R, V, k = w.B * 10, w.V, 10
+    g = torch.Generator(device=dev)
+    g.manual_seed(shard_seed(args.seed, rank))
+    logits = wl.empty_rows((R, V), torch.bfloat16, dev)
+    logits.copy_(torch.randn((R, V), generator=g, device=dev) * 3)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        binding.draft_topk(logits, k, 1.0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        binding.draft_topk(logits, k, 1.0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+
+    # end to end: the rows from pinned host memory in, children and confidences back
+    host = logits.cpu().pin_memory()
+    dbuf = torch.empty_like(logits)
+
+    def e2e_step():
+        dbuf.copy_(host, non_blocking=True)
+        out = binding.draft_topk(dbuf, k, 1.0)
+        return {a: v.to("cpu", non_blocking=True) for a, v in out.items()}
+
+    for _ in range(2):
+        res = e2e_step()
+    torch.cuda.synchronize()
+    h2d = host.numel() * host.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in res.values())
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.e2e_steps
+    peaks, peak_kind = load_peaks()
+    bytes_launch = R * V * 2
+    gbs = bytes_launch / (ms / 1e3) / 1e9
+    line = {"metric": "draft-side top-k drafting: expanded-node rows per second",
+            "value": world * R / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"draft_topk_r{R}_v{V}_k{k}", "rows": R, "V": V, "k": k,
+                       "temperature": 1.0, "l2": f"rows {bytes_launch / 1e6:.0f} MB, larger than L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "kernel": "draft_topk_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_ms": ms},
+            "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, inp, dev, stream):
     """The same metric through the public C-ABI call with host buffers: every step
     copies the inputs host->device from pinned memory, verifies, and copies the
@@ -736,6 +811,8 @@ def main():
         run_commit(args)
     elif args.op == "tree":
         run_tree(args)
+    elif args.op == "draft":
+        run_draft(args)
     else:
         run_ours(args)
 

@@ -363,6 +363,25 @@ int spec_verify_tree_per_request(uint32_t phases, const void* logits_p, const vo
                                  size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * Draft-side top-k drafting (EAGLE / EAGLE-2 paper translation, modelers.csdn.net,
+ * sections 2.3.1-2.3.2; "LLM speculative decoding: EAGLE", jingming.pro, 4.2.1): for
+ * each of R rows of draft logits (a node the draft model expands), the k largest
+ * tokens (ties to the lower index, listed in that order) and their confidences, the
+ * softmax probability at `temperature` over the whole row.  These are the children
+ * (cand_token) and confidences (cand_prob) the dynamic tree below ranks.
+ *   logits: device, [R, row_pitch] of dtype, base and row_pitch * sizeof(elem) 16-byte
+ *   aligned; out_tokens [R, k] int32, out_probs [R, k] float32, out_status [R] int32
+ *   (optional): SPEC_ROW_NONFINITE for a row holding NaN or +inf or all -inf (its
+ *   tokens -1 and confidences 0), else SPEC_TREE_OK.
+ *   1 <= k <= 32 and k <= V; temperature finite and > 0.
+ * Errors: SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED_DTYPE, SPEC_ERR_MISALIGNED,
+ * SPEC_ERR_TOO_LARGE (V > SPEC_MAX_VOCAB), SPEC_ERR_CUDA.
+ */
+int spec_draft_topk(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
+                    int64_t row_pitch, int32_t k, float temperature, int32_t* out_tokens,
+                    float* out_probs, int32_t* out_status, spec_stream_t stream);
+
+/*
  * EAGLE-2 dynamic draft tree (EAGLE / EAGLE-2 paper translation, modelers.csdn.net,
  * sections 2.3.1-2.3.2; "LLM speculative decoding: EAGLE", jingming.pro, 4.2.1).
  * The draft model's candidates of tree b are given in creation order (layer by layer):

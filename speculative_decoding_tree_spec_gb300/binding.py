@@ -104,6 +104,9 @@ def lib():
                 P, P, i32, P, P, P, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_uint64,
                 P, P, P, P, P, P, P, ctypes.c_size_t, P]
             L.spec_verify_tree_per_request.restype = ctypes.c_int
+            L.spec_draft_topk.argtypes = [P, ctypes.c_int, i32, i32, ctypes.c_int64, i32,
+                                          ctypes.c_float, P, P, P, P]
+            L.spec_draft_topk.restype = ctypes.c_int
             L.spec_tree_expand_topk.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
             L.spec_tree_expand_topk.restype = ctypes.c_int
             L.spec_tree_build.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P]
@@ -380,6 +383,25 @@ def commit_accepted_path(cache: torch.Tensor, prefix_len: torch.Tensor, accepted
         accept_len.data_ptr(), accepted_path.shape[1], _stream_ptr(stream))
     if rc != 0:
         raise SpecError(rc, "spec_commit_accepted_path")
+
+
+def draft_topk(logits: torch.Tensor, k: int, temperature: float = 1.0, stream=None) -> dict:
+    """spec_draft_topk on [R, V] device rows (row pitch from the tensor's stride):
+    tokens [R, k] int32, probs [R, k] float32, status [R] int32."""
+    R, V = logits.shape
+    if logits.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    dev = logits.device
+    out = {"tokens": torch.empty((R, k), dtype=torch.int32, device=dev),
+           "probs": torch.empty((R, k), dtype=torch.float32, device=dev),
+           "status": torch.empty(R, dtype=torch.int32, device=dev)}
+    rc = lib().spec_draft_topk(logits.data_ptr(), _dtype_code(logits), R, V, logits.stride(0), k,
+                               float(temperature), out["tokens"].data_ptr(),
+                               out["probs"].data_ptr(), out["status"].data_ptr(),
+                               _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_draft_topk")
+    return out
 
 
 def tree_expand_topk(cand_parent: torch.Tensor, cand_prob: torch.Tensor, layer_begin: int,

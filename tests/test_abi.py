@@ -179,3 +179,17 @@ def test_per_request_validation(L):
     assert f(*args(B=0)) == 0                     # no trees: nothing launched
     assert f(*args(T=None)) == -1                 # the temperatures are required
     assert f(*args(q=None)) == -1                 # the draft logits are required
+
+
+def test_draft_topk_validation(L):
+    f = L.spec_draft_topk
+    assert f(FAKE, 1, 0, 100, 104, 10, 1.0, FAKE, FAKE, None, None) == 0   # no rows
+    assert f(FAKE, 1, 4, 100, 104, 0, 1.0, FAKE, FAKE, None, None) == -1   # k = 0
+    assert f(FAKE, 1, 4, 100, 104, 33, 1.0, FAKE, FAKE, None, None) == -1  # k above 32
+    assert f(FAKE, 1, 4, 8, 8, 9, 1.0, FAKE, FAKE, None, None) == -1       # k above V
+    assert f(FAKE, 1, 4, 100, 104, 10, 0.0, FAKE, FAKE, None, None) == -1  # T = 0
+    assert f(FAKE, 1, 4, 100, 104, 10, float("nan"), FAKE, FAKE, None, None) == -1
+    assert f(FAKE, 1, 4, 100, 99, 10, 1.0, FAKE, FAKE, None, None) == -1   # pitch < V
+    assert f(FAKE, 1, 4, 100, 100, 10, 1.0, FAKE, FAKE, None, None) == -3  # 200-byte pitch
+    assert f(FAKE, 3, 4, 100, 104, 10, 1.0, FAKE, FAKE, None, None) == -2  # dtype
+    assert f(None, 1, 4, 100, 104, 10, 1.0, FAKE, FAKE, None, None) == -1

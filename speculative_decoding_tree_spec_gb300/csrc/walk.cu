@@ -34,7 +34,6 @@ constexpr int GT = kWalkThreads;          // greedy walk block
 constexpr int CT = kClusterWalkThreads;   // sampling walk CTA
 constexpr int CW = CT / 32;
 constexpr int kMaxC = kMaxWalkCluster;
-constexpr int kUnitsInFlight = 2;          // units of each row a thread loads before using them
 constexpr uint64_t kExchangeLimitNs = 2000000000ull;
 constexpr int kSlotW = 16;     // 64-bit words one CTA can push in one exchange
 constexpr int kCandCTA = 512;  // window candidates one CTA keeps per row
@@ -317,6 +316,20 @@ __device__ __forceinline__ void filter_unit(uint4& raw, int x0, const RowF& f, f
   raw = make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// True when every token of the unit lies strictly below the cut value, so that none
+// is kept and its filtered probabilities are all exactly 0 (NaN never counts as
+// below).  With top-k / top-p most units of a row are skipped this way.
+__device__ __forceinline__ bool unit_below(const uint4& raw, const RowF& f, uint16_t) {
+  const __nv_bfloat162 m2 = __hmax2(__hmax2(as_bf2(raw.x), as_bf2(raw.y)),
+                                    __hmax2(as_bf2(raw.z), as_bf2(raw.w)));
+  return __hlt2_mask(m2, as_bf2(f.zc2)) == 0xffffffffu;
+}
+__device__ __forceinline__ bool unit_below(const uint4& raw, const RowF& f, float) {
+  const float m = fmaxf(fmaxf(__uint_as_float(raw.x), __uint_as_float(raw.y)),
+                        fmaxf(__uint_as_float(raw.z), __uint_as_float(raw.w)));
+  return m < f.zc;
+}
+
 // Filtered probabilities of one unit: 2^((z - m) c) * inv_s, evaluated with the
 // same roundings as the dense row pass's weights.
 template <typename T>
@@ -359,6 +372,11 @@ __device__ __forceinline__ float dist_from_raw(uint4 rp, uint4 rq, int u, const 
                                                const RowF& fq, int j, const float* invz,
                                                float (&val)[Elt<T>::kPerUnit]) {
   constexpr int E = Elt<T>::kPerUnit;
+  if (unit_below(rp, fp, T())) {  // p (and so every residual of it) is 0 here
+#pragma unroll
+    for (int e = 0; e < E; ++e) val[e] = 0.f;
+    return 0.f;
+  }
   unit_probs<T>(rp, u * E, fp, val);
   if (j > 0) {
     float q[E];
@@ -477,11 +495,73 @@ struct CShared {
   int st_arg[2][CW];
   int st_bad[2];
   SelShared sel;
+  uint4* ring;      // the slice-streaming ring (dynamic shared memory)
+  int ring_stages;  // its depth: 4, or 2 where shared memory is short
 };
 
 struct BSync {
   __device__ static void sync() { __syncthreads(); }
 };
+
+// Slice streaming: each thread copies its own units of one or two rows into its own
+// slots of a shared-memory ring with cp.async (kRingUnits units of each row per stage,
+// S stages in flight) and reads back only those slots, so no block barrier is needed
+// and the copies in flight cost no registers.  body(u, raw0, raw1) sees every unit u
+// of [ua, ub) of both rows (raw1 repeats raw0 when nrows is 1), in increasing u per
+// thread.
+constexpr int kRingUnits = 2;
+constexpr size_t ring_bytes(int stages) { return (size_t)stages * kRingUnits * 2 * CT * 16; }
+
+template <typename T, int S, typename Body>
+__device__ __forceinline__ void stream_slice_s(const void* const (&rows)[2], int nrows, int V,
+                                               int ua, int ub, uint4* ring, Body&& body) {
+  constexpr int E = Elt<T>::kPerUnit;
+  const int span = CT * kRingUnits;
+  const int niter = (ub - ua + span - 1) / span;  // the same for every thread
+  auto slot = [&](int st, int k, int r) {
+    return ring + ((st * kRingUnits + k) * 2 + r) * CT + threadIdx.x;
+  };
+  auto issue = [&](int it) {
+    if (it < niter) {
+      const int st = it % S;
+#pragma unroll
+      for (int k = 0; k < kRingUnits; ++k) {
+        const int u = ua + (int)threadIdx.x + it * span + k * CT;
+        if (u >= ub) continue;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (r >= nrows) break;
+          if ((u + 1) * E <= V) cp_async16(slot(st, k, r), reinterpret_cast<const uint4*>(rows[r]) + u);
+          else *slot(st, k, r) = load_raw<T>(rows[r], V, u);  // the partial last unit
+        }
+      }
+    }
+    cp_async_commit();  // every thread commits every group: the counts stay aligned
+  };
+#pragma unroll
+  for (int it = 0; it < S - 1; ++it) issue(it);
+  for (int it = 0; it < niter; ++it) {
+    issue(it + S - 1);
+    cp_async_wait<S - 1>();
+    const int st = it % S;
+#pragma unroll
+    for (int k = 0; k < kRingUnits; ++k) {
+      const int u = ua + (int)threadIdx.x + it * span + k * CT;
+      if (u >= ub) break;
+      const uint4 r0 = *slot(st, k, 0);
+      const uint4 r1 = nrows > 1 ? *slot(st, k, 1) : r0;
+      body(u, r0, r1);
+    }
+  }
+  cp_async_wait<0>();
+}
+
+template <typename T, typename Body>
+__device__ __forceinline__ void stream_slice(const void* const (&rows)[2], int nrows, int V,
+                                             int ua, int ub, const CShared& sh, Body&& body) {
+  if (sh.ring_stages == 4) stream_slice_s<T, 4>(rows, nrows, V, ua, ub, sh.ring, body);
+  else stream_slice_s<T, 2>(rows, nrows, V, ua, ub, sh.ring, body);
+}
 
 // Cluster exchange: every CTA pushes nv words (thread 0's v) into slot[set][rank]
 // of every CTA and arrives on that CTA's mbarrier; once the local mbarrier
@@ -547,34 +627,22 @@ __device__ double block_sum_ff(FF v, CShared& sh) {
 // max(0, p^(j) - q).
 template <typename T>
 __device__ FF residual_partial(const void* prow, const void* qrow, int V, int ua, int ub,
-                               const RowF& fp, const RowF& fq, int j, const float* invz) {
+                               const RowF& fp, const RowF& fq, int j, const float* invz,
+                               const CShared& sh) {
   constexpr int E = Elt<T>::kPerUnit;
   FF acc;
-  for (int u0 = ua + threadIdx.x; u0 < ub; u0 += CT * kUnitsInFlight) {
-    uint4 rp[kUnitsInFlight], rq[kUnitsInFlight];
-#pragma unroll
-    for (int k = 0; k < kUnitsInFlight; ++k) {
-      const int u = u0 + k * CT;
-      if (u < ub) {
-        rp[k] = load_raw<T>(prow, V, u);
-        rq[k] = load_raw<T>(qrow, V, u);
-      }
-    }
+  const void* const rows[2] = {prow, qrow};
+  stream_slice<T>(rows, 2, V, ua, ub, sh, [&](int u, const uint4& rp, const uint4& rq) {
+    if (unit_below(rp, fp, T())) return;  // p is 0 on the unit: max(0, p - q) too
+    float p[E], q[E];
+    unit_probs<T>(rp, u * E, fp, p);
+    unit_probs<T>(rq, u * E, fq, q);
+    residual_chain<E>(p, q, j, invz);
     float part = 0.f;
 #pragma unroll
-    for (int k = 0; k < kUnitsInFlight; ++k) {
-      const int u = u0 + k * CT;
-      if (u < ub) {
-        float p[E], q[E];
-        unit_probs<T>(rp[k], u * E, fp, p);
-        unit_probs<T>(rq[k], u * E, fq, q);
-        residual_chain<E>(p, q, j, invz);
-#pragma unroll
-        for (int e = 0; e < E; ++e) part += fmaxf(0.f, __fsub_rn(p[e], q[e]));
-      }
-    }
+    for (int e = 0; e < E; ++e) part += fmaxf(0.f, __fsub_rn(p[e], q[e]));
     acc.add(part);
-  }
+  });
   return acc;
 }
 
@@ -760,47 +828,34 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
                                unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
                                CShared& sh) {
   constexpr int E = Elt<T>::kPerUnit;
-  constexpr int kBatch = 2;  // units of each row loaded before any is used
-  for (int u0 = ua + threadIdx.x; u0 < ub; u0 += CT * kBatch) {
-  uint4 rb[2][kBatch];
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (r < nrows && u0 + k * CT < ub) rb[r][k] = load_raw<T>(rows[r], V, u0 + k * CT);
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int u = u0 + k * CT;
-    if (u >= ub) break;
+  stream_slice<T>(rows, nrows, V, ua, ub, sh, [&](int u, const uint4& raw0, const uint4& raw1) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;
       float z[E];
-      Elt<T>::unpack(rb[r][k], z);
+      Elt<T>::unpack(r ? raw1 : raw0, z);
       float mx = z[0];
 #pragma unroll
       for (int e = 1; e < E; ++e) mx = fmaxf(mx, z[e]);
-      if (mx >= thr[r]) {
+      if (mx < thr[r]) continue;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if (z[e] >= thr[r]) {
-            const uint32_t k = order_key(z[e]);
-            // once the list is full only the overflow matters: stop counting
-            if (*((volatile unsigned*)&sh.ncand[r]) <= (unsigned)kCandCTA) {
-              const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
-              if (pos < (unsigned)kCandCTA)
-                cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
-            }
-            if (hist[r]) {
-              const uint32_t bin = k16m[r] - (k >> 16);
-              if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
-            }
+      for (int e = 0; e < E; ++e) {
+        if (z[e] >= thr[r]) {
+          const uint32_t k = order_key(z[e]);
+          // once the list is full only the overflow matters: stop counting
+          if (*((volatile unsigned*)&sh.ncand[r]) <= (unsigned)kCandCTA) {
+            const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
+            if (pos < (unsigned)kCandCTA)
+              cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
+          }
+          if (hist[r]) {
+            const uint32_t bin = k16m[r] - (k >> 16);
+            if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
           }
         }
       }
     }
-  }
-  }
+  });
 }
 
 // Step 2 after the sort: the cut from n sorted candidates (descending, padded to
@@ -1553,7 +1608,7 @@ __device__ Samp tree_samp(const TreeJob& job, int b, int& status) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJob job, int C, int max_steps) {
+__global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJob job, int C, int max_steps, int ring_stages) {
   __shared__ CShared sh;
   // parents [N], tokens [N], child offsets [N+1], children [N]; then Z [N] (fp64),
   // 1/Z [N] and the per-warp step totals [CW][max_steps]
@@ -1569,6 +1624,8 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   // the top-k / top-p cut's buffers (16-byte aligned)
   unsigned char* cut_smem = reinterpret_cast<unsigned char*>(
       reinterpret_cast<uintptr_t>(steps + CW * max_steps + 3) & ~(uintptr_t)15);
+  // the streaming ring follows the cut's buffers (16-byte aligned: both sizes are)
+  uint4* ring = reinterpret_cast<uint4*>(cut_smem + (job.trunc ? cut_smem_bytes<T>() : 0));
   int status = SPEC_TREE_OK;
   {
     const Samp s0 = tree_samp(job, b, status);
@@ -1582,6 +1639,8 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     mbar_init(&sh.xbar[0], (uint32_t)C);
     mbar_init(&sh.xbar[1], (uint32_t)C);
     sh.err = 0u;
+    sh.ring = ring;
+    sh.ring_stages = ring_stages;
     fence_barrier_init();
   }
   cluster_sync_all();
@@ -1705,7 +1764,7 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       __syncthreads();
       if (acc) { next = ch; break; }
       const double part = block_sum_ff(
-          residual_partial<T>(prow, qrow, V, ua, ub, fp, fq, j, invz), sh);
+          residual_partial<T>(prow, qrow, V, ua, ub, fp, fq, j, invz, sh), sh);
       double z;
       if (!cluster_sum(part, sh, C, rank, n_ex, z, nullptr)) { timed_out = true; break; }
       if (threadIdx.x == 0) {
@@ -1802,7 +1861,18 @@ cudaError_t launch_sampling(const TreeJob& job, cudaStream_t s) {
   const int max_steps = max(1, ((slice + CW - 1) / CW + 31) / 32);
   size_t dyn = tree_smem_bytes(job.N) + (size_t)job.N * (sizeof(double) + sizeof(float)) +
                (size_t)CW * max_steps * sizeof(float);
-  if (job.trunc) dyn += 16 + cut_smem_bytes<T>();  // 16-byte alignment + the cut's buffers
+  dyn += 16;                                       // 16-byte alignment of what follows
+  if (job.trunc) dyn += cut_smem_bytes<T>();       // the cut's buffers
+  // the streaming ring: 4 stages where two CTAs per SM still fit, else 2
+  static int static_bytes = -1;
+  if (static_bytes < 0) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, cluster_walk_kernel<T>) != cudaSuccess) return cudaErrorInvalidValue;
+    static_bytes = (int)fa.sharedSizeBytes;
+  }
+  const size_t two_per_sm = 233472 / kWalkCtasPerSm - 1024;
+  const int ring_stages = (dyn + ring_bytes(4) + (size_t)static_bytes <= two_per_sm) ? 4 : 2;
+  dyn += ring_bytes(ring_stages);
   if (dyn > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         cluster_walk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
@@ -1820,7 +1890,7 @@ cudaError_t launch_sampling(const TreeJob& job, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cluster_walk_kernel<T>, job, C, max_steps);
+  return cudaLaunchKernelEx(&cfg, cluster_walk_kernel<T>, job, C, max_steps, ring_stages);
 }
 
 }  // namespace

@@ -506,9 +506,10 @@ struct BSync {
 // Slice streaming: each thread copies its own units of one or two rows into its own
 // slots of a shared-memory ring with cp.async (kRingUnits units of each row per stage,
 // S stages in flight) and reads back only those slots, so no block barrier is needed
-// and the copies in flight cost no registers.  body(u, raw0, raw1) sees every unit u
-// of [ua, ub) of both rows (raw1 repeats raw0 when nrows is 1), in increasing u per
-// thread.
+// and the copies in flight cost no registers.  body(u, valid, raw0, raw1) is called by
+// every thread the same number of times (so a body may use warp collectives); with
+// valid set it sees unit u of both rows (raw1 repeats raw0 when nrows is 1), every unit
+// of [ua, ub) once, in increasing u per thread.
 constexpr int kRingUnits = 2;
 constexpr size_t ring_bytes(int stages) { return (size_t)stages * kRingUnits * 2 * CT * 16; }
 
@@ -547,10 +548,13 @@ __device__ __forceinline__ void stream_slice_s(const void* const (&rows)[2], int
 #pragma unroll
     for (int k = 0; k < kRingUnits; ++k) {
       const int u = ua + (int)threadIdx.x + it * span + k * CT;
-      if (u >= ub) break;
-      const uint4 r0 = *slot(st, k, 0);
-      const uint4 r1 = nrows > 1 ? *slot(st, k, 1) : r0;
-      body(u, r0, r1);
+      const bool valid = u < ub;
+      uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+      if (valid) {
+        r0 = *slot(st, k, 0);
+        r1 = nrows > 1 ? *slot(st, k, 1) : r0;
+      }
+      body(u, valid, r0, r1);
     }
   }
   cp_async_wait<0>();
@@ -590,7 +594,11 @@ __device__ const SlotRow* cluster_share(const uint64_t* v, int nv, CShared& sh, 
       arrive_peer(peer_addr(&sh.xbar[set], t));
     }
   }
-  const bool ok = __syncthreads_and(mbar_wait_cluster(&sh.xbar[set], parity, kExchangeLimitNs));
+  // one thread waits (a spinning CTA would take issue slots from the other tree on
+  // its SM); the barrier then orders its acquire before every thread's reads
+  bool got = true;
+  if (threadIdx.x == 0) got = mbar_wait_cluster(&sh.xbar[set], parity, kExchangeLimitNs);
+  const bool ok = __syncthreads_and(got);
   return ok ? sh.slot[set] : nullptr;
 }
 
@@ -632,8 +640,8 @@ __device__ FF residual_partial(const void* prow, const void* qrow, int V, int ua
   constexpr int E = Elt<T>::kPerUnit;
   FF acc;
   const void* const rows[2] = {prow, qrow};
-  stream_slice<T>(rows, 2, V, ua, ub, sh, [&](int u, const uint4& rp, const uint4& rq) {
-    if (unit_below(rp, fp, T())) return;  // p is 0 on the unit: max(0, p - q) too
+  stream_slice<T>(rows, 2, V, ua, ub, sh, [&](int u, bool valid, const uint4& rp, const uint4& rq) {
+    if (!valid || unit_below(rp, fp, T())) return;  // p is 0 on the unit: max(0, p - q) too
     float p[E], q[E];
     unit_probs<T>(rp, u * E, fp, p);
     unit_probs<T>(rq, u * E, fq, q);
@@ -828,30 +836,42 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
                                unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
                                CShared& sh) {
   constexpr int E = Elt<T>::kPerUnit;
-  stream_slice<T>(rows, nrows, V, ua, ub, sh, [&](int u, const uint4& raw0, const uint4& raw1) {
+  const int lane = threadIdx.x & 31;
+  stream_slice<T>(rows, nrows, V, ua, ub, sh,
+                  [&](int u, bool valid, const uint4& raw0, const uint4& raw1) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;
       float z[E];
       Elt<T>::unpack(r ? raw1 : raw0, z);
-      float mx = z[0];
+      unsigned bits = 0u;  // window members of this lane's unit
+      if (valid) {
 #pragma unroll
-      for (int e = 1; e < E; ++e) mx = fmaxf(mx, z[e]);
-      if (mx < thr[r]) continue;
+        for (int e = 0; e < E; ++e) bits |= (unsigned)(z[e] >= thr[r]) << e;
+      }
+      if (!__any_sync(kFull, bits != 0u)) continue;
+      // one list reservation per warp: offsets from a warp scan of the lanes' counts
+      const unsigned mine = __popc(bits);
+      unsigned incl = mine;
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        if (z[e] >= thr[r]) {
-          const uint32_t k = order_key(z[e]);
-          // once the list is full only the overflow matters: stop counting
-          if (*((volatile unsigned*)&sh.ncand[r]) <= (unsigned)kCandCTA) {
-            const unsigned pos = atomicAdd(&sh.ncand[r], 1u);
-            if (pos < (unsigned)kCandCTA)
-              cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
-          }
-          if (hist[r]) {
-            const uint32_t bin = k16m[r] - (k >> 16);
-            if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
-          }
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned total = __shfl_sync(kFull, incl, 31);
+      unsigned base = 0u;
+      if (lane == 0) base = atomicAdd(&sh.ncand[r], total);
+      base = __shfl_sync(kFull, base, 0) + incl - mine;
+      while (bits) {
+        const int e = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const uint32_t k = order_key(z[e]);
+        if (base < (unsigned)kCandCTA)
+          cand[r][base] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
+        ++base;
+        if (hist[r]) {
+          const uint32_t bin = k16m[r] - (k >> 16);
+          if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
         }
       }
     }

@@ -188,6 +188,11 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+DRAFT_SOURCES = ["speculative_decoding_tree_spec_gb300/csrc/draft.cu",
+                 "speculative_decoding_tree_spec_gb300/csrc/common.cuh",
+                 "speculative_decoding_tree_spec_gb300/csrc/internal.h"]
+
+
 def sources_digest(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -196,18 +201,19 @@ def sources_digest(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """Per-launch DRAM traffic of the row pass from the committed ncu summary, if it was
-    captured on the current row-pass sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"row_pass_{workload}.md")
+def profiled_traffic(workload: str, profile: str = "row_pass", sources=None):
+    """Per-launch DRAM traffic of a kernel from its committed ncu summary
+    (profiles/<profile>_<workload>.md), if it was captured on the kernel's current
+    sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{profile}_{workload}.md")
     if not os.path.exists(path):
         return None, None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    d = re.search(r"row_pass_sources_sha256_16:\s*([0-9a-f]+)", text)
+    d = re.search(r"sources_sha256_16:\s*([0-9a-f]+)", text)
     if not m or not d:
         return None, None
-    if d.group(1) != sources_digest(ROW_PASS_SOURCES):
+    if d.group(1) != sources_digest(sources or ROW_PASS_SOURCES):
         return None, "stale"
     return float(m.group(1)), "current"
 
@@ -725,6 +731,7 @@ def run_draft(args):
     peaks, peak_kind = load_peaks()
     bytes_launch = R * V * 2
     gbs = bytes_launch / (ms / 1e3) / 1e9
+    traffic, _ = profiled_traffic(f"r{R}_v{V}_k{k}", "draft_topk", DRAFT_SOURCES)
     line = {"metric": "draft-side top-k drafting: expanded-node rows per second",
             "value": world * R / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -733,7 +740,7 @@ def run_draft(args):
             "config": {"workload": f"draft_topk_r{R}_v{V}_k{k}", "rows": R, "V": V, "k": k,
                        "temperature": 1.0, "l2": f"rows {bytes_launch / 1e6:.0f} MB, larger than L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
-                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": traffic,
                          "kernel": "draft_topk_kernel", "peak_source": f"{peak_kind} hbm_gbs",
                          "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_ms": ms},
             "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s",

@@ -63,6 +63,9 @@ def parse_args():
                     help="commit: time the accepted-path commit on a KV cache instead; tree: "
                          "the EAGLE-2 dynamic draft-tree build (expansion + rerank + mask); "
                          "draft: the draft-side top-k drafting of the expanded nodes' rows")
+    ap.add_argument("--fused", action="store_true",
+                    help="with --op draft: the draft LM head + top-k in one call (features x "
+                         "weight on the tensor cores, then the ranking kernel)")
     ap.add_argument("--visited-only", action="store_true",
                     help="the visited-rows-only schedule (no dense pass); reported as its own "
                          "line, not the dense schedule's number")
@@ -750,6 +753,86 @@ def run_draft(args):
         print(json.dumps(line), flush=True)
 
 
+def run_draft_fused(args):
+    """Draft LM head + top-k in one call: the features of the nodes one EAGLE-2 layer
+    expands (the workload's batch x 10, d = 4096, N(0, 1)) times a draft LM-head weight
+    (V x 4096, N(0, 0.02^2)) on the tensor cores, the bf16 logits ranked by the top-k
+    kernel (k = 10, T = 1).  Rows per second and the tensor roofline of the call."""
+    from speculative_decoding_tree_spec_gb300 import binding
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    w = wl.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    R, V, d, k = w.B * 10, w.V, 4096, 10
+    g = torch.Generator(device=dev)
+    g.manual_seed(shard_seed(args.seed, rank))
+    feats = torch.randn((R, d), generator=g, device=dev).to(torch.bfloat16)
+    weight = (torch.randn((V, d), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    ws = torch.empty(int(binding.lib().spec_draft_fused_workspace_size(R, V, k)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        binding.draft_topk_fused_lmhead(feats, weight, k, 1.0, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        binding.draft_topk_fused_lmhead(feats, weight, k, 1.0, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+
+    # end to end: the features from pinned host memory in, children and confidences back
+    # (the weight stays resident, as a model's weights do)
+    host = feats.cpu().pin_memory()
+    dbuf = torch.empty_like(feats)
+
+    def e2e_step():
+        dbuf.copy_(host, non_blocking=True)
+        out = binding.draft_topk_fused_lmhead(dbuf, weight, k, 1.0, workspace=ws)
+        return {a: v.to("cpu", non_blocking=True) for a, v in out.items()}
+
+    for _ in range(2):
+        res = e2e_step()
+    torch.cuda.synchronize()
+    h2d = host.numel() * host.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in res.values())
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.e2e_steps
+    peaks, peak_kind = load_peaks()
+    flops = 2.0 * R * V * d
+    tf = flops / (ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    line = {"metric": "draft LM head + top-k drafting in one call: expanded-node rows per second",
+            "value": world * R / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"draft_lmhead_topk_r{R}_v{V}_d{d}_k{k}", "rows": R, "V": V,
+                       "d": d, "k": k, "temperature": 1.0,
+                       "logits": "bf16 rows in the workspace, read back by the ranking kernel"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "traffic": None,
+                         "kernel": "lmhead_kernel + draft_topk_kernel (whole call)",
+                         "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                         "algorithmic_flops_per_launch": flops, "avg_launch_ms": ms},
+            "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * 2}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, inp, dev, stream):
     """The same metric through the public C-ABI call with host buffers: every step
     copies the inputs host->device from pinned memory, verifies, and copies the
@@ -818,6 +901,8 @@ def main():
         run_commit(args)
     elif args.op == "tree":
         run_tree(args)
+    elif args.op == "draft" and args.fused:
+        run_draft_fused(args)
     elif args.op == "draft":
         run_draft(args)
     else:

@@ -382,6 +382,26 @@ int spec_draft_topk(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
                     float* out_probs, int32_t* out_status, spec_stream_t stream);
 
 /*
+ * Draft LM head + top-k in one call: spec_draft_topk on draft logits formed here,
+ * F W^T, from the expanded nodes' draft features F [R, d] (bf16, row-major, device) and
+ * the draft LM-head weight W [V, d] (bf16, row-major, device) on the tensor cores.  The
+ * bf16 logits go to out_logits [R, logits_pitch] when given (else to the workspace).
+ * The children are the k largest of the bf16-rounded logits (ties to the lower index),
+ * their confidences the softmax at `temperature` over the row.  1 <= k <= 32, k <= V;
+ * d a multiple of 8 and both bases 16-byte aligned (else SPEC_ERR_MISALIGNED).
+ * workspace: device, 256-byte aligned, spec_draft_fused_workspace_size(R, V, k) bytes
+ * (it holds the logits rows: about 2 R V bytes).
+ * Other outputs and errors as spec_draft_topk; a device wait that gave up reports
+ * SPEC_ROW_TIMEOUT for every row.
+ */
+size_t spec_draft_fused_workspace_size(int32_t R, int32_t V, int32_t k);
+int spec_draft_topk_fused_lmhead(const void* features, const void* lm_head_w, int32_t d,
+                                 int32_t R, int32_t V, int32_t k, float temperature,
+                                 void* out_logits, int64_t logits_pitch, int32_t* out_tokens,
+                                 float* out_probs, int32_t* out_status, void* workspace,
+                                 size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * EAGLE-2 dynamic draft tree (EAGLE / EAGLE-2 paper translation, modelers.csdn.net,
  * sections 2.3.1-2.3.2; "LLM speculative decoding: EAGLE", jingming.pro, 4.2.1).
  * The draft model's candidates of tree b are given in creation order (layer by layer):

@@ -107,6 +107,12 @@ def lib():
             L.spec_draft_topk.argtypes = [P, ctypes.c_int, i32, i32, ctypes.c_int64, i32,
                                           ctypes.c_float, P, P, P, P]
             L.spec_draft_topk.restype = ctypes.c_int
+            L.spec_draft_fused_workspace_size.argtypes = [i32, i32, i32]
+            L.spec_draft_fused_workspace_size.restype = ctypes.c_size_t
+            L.spec_draft_topk_fused_lmhead.argtypes = [P, P, i32, i32, i32, i32, ctypes.c_float,
+                                                       P, ctypes.c_int64, P, P, P, P,
+                                                       ctypes.c_size_t, P]
+            L.spec_draft_topk_fused_lmhead.restype = ctypes.c_int
             L.spec_tree_expand_topk.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
             L.spec_tree_expand_topk.restype = ctypes.c_int
             L.spec_tree_build.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P]
@@ -401,6 +407,40 @@ def draft_topk(logits: torch.Tensor, k: int, temperature: float = 1.0, stream=No
                                _stream_ptr(stream))
     if rc != 0:
         raise SpecError(rc, "spec_draft_topk")
+    return out
+
+
+def draft_topk_fused_lmhead(features: torch.Tensor, weight: torch.Tensor, k: int,
+                            temperature: float = 1.0, want_logits: bool = False, workspace=None,
+                            stream=None) -> dict:
+    """spec_draft_topk_fused_lmhead: features [R, d] and weight [V, d] bf16 (device,
+    contiguous).  Returns tokens [R, k], probs [R, k], status [R] and, if asked, the
+    bf16 logits [R, V] (a padded-pitch view)."""
+    R, d = features.shape
+    V, d2 = weight.shape
+    if d2 != d or features.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("features [R, d] and weight [V, d] must be bf16 with the same d")
+    if not (features.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("features and weight must be contiguous")
+    dev = features.device
+    out = {"tokens": torch.empty((R, k), dtype=torch.int32, device=dev),
+           "probs": torch.empty((R, k), dtype=torch.float32, device=dev),
+           "status": torch.empty(R, dtype=torch.int32, device=dev)}
+    logits, pitch = None, 0
+    if want_logits:
+        pitch = (V + 7) // 8 * 8  # rows on 16-byte boundaries
+        logits = torch.empty((R, pitch), dtype=torch.bfloat16, device=dev)[:, :V]
+        out["logits"] = logits
+    ws_bytes = int(lib().spec_draft_fused_workspace_size(R, V, k))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    rc = lib().spec_draft_topk_fused_lmhead(
+        features.data_ptr(), weight.data_ptr(), d, R, V, k, float(temperature),
+        None if logits is None else logits.data_ptr(), pitch, out["tokens"].data_ptr(),
+        out["probs"].data_ptr(), out["status"].data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream_ptr(stream))
+    if rc != 0:
+        raise SpecError(rc, "spec_draft_topk_fused_lmhead")
     return out
 
 

@@ -37,6 +37,7 @@ struct DraftJob {
   int32_t* out_tok;
   float* out_prob;
   int32_t* out_status;
+  const int* err;  // the producing GEMM's error flag, or null
 };
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
@@ -325,7 +326,8 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
     job.out_prob[(int64_t)r * k_out + t] = p;
   }
   if (threadIdx.x == 0 && job.out_status)
-    job.out_status[r] = finite ? SPEC_TREE_OK : SPEC_ROW_NONFINITE;
+    job.out_status[r] = (job.err && *job.err) ? SPEC_ROW_TIMEOUT
+                                              : (finite ? SPEC_TREE_OK : SPEC_ROW_NONFINITE);
 }
 
 template <typename T>
@@ -342,10 +344,11 @@ cudaError_t launch_draft(const DraftJob& job, cudaStream_t s) {
 
 using namespace svk;
 
-extern "C" int spec_draft_topk(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
-                               int64_t row_pitch, int32_t k, float temperature,
-                               int32_t* out_tokens, float* out_probs, int32_t* out_status,
-                               spec_stream_t stream) {
+namespace {
+
+int draft_topk_impl(const void* logits, spec_dtype dtype, int32_t R, int32_t V, int64_t row_pitch,
+                    int32_t k, float temperature, int32_t* out_tokens, float* out_probs,
+                    int32_t* out_status, const int* err, spec_stream_t stream) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED_DTYPE;
   if (R < 0 || V < 1 || k < 1 || k > kDraftMaxK || k > V) return SPEC_ERR_INVALID_ARG;
   if (V > SPEC_MAX_VOCAB) return SPEC_ERR_TOO_LARGE;
@@ -367,8 +370,89 @@ extern "C" int spec_draft_topk(const void* logits, spec_dtype dtype, int32_t R, 
   job.out_tok = out_tokens;
   job.out_prob = out_probs;
   job.out_status = out_status;
+  job.err = err;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e =
       dtype == SPEC_BF16 ? launch_draft<uint16_t>(job, s) : launch_draft<float>(job, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int spec_draft_topk(const void* logits, spec_dtype dtype, int32_t R, int32_t V,
+                               int64_t row_pitch, int32_t k, float temperature,
+                               int32_t* out_tokens, float* out_probs, int32_t* out_status,
+                               spec_stream_t stream) {
+  return draft_topk_impl(logits, dtype, R, V, row_pitch, k, temperature, out_tokens, out_probs,
+                         out_status, nullptr, stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// Draft LM head + top-k in one call: the draft logits F W^T of the expanded nodes are
+// formed on the tensor cores (the LM-head GEMM of lmhead.cu, bf16 rows written once)
+// and ranked by the kernel above.  Ranking inside the GEMM's epilogue (one row per
+// epilogue thread, a register list per row and tile) was measured 2.2x slower than
+// this pair: the list upkeep outlasted the tile's MMAs.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+struct DraftFusedLayout {
+  size_t part, err, logits, total;
+  int64_t pitch;  // of the logits rows kept in the workspace
+};
+
+DraftFusedLayout draft_fused_layout(int32_t R, int32_t V) {
+  DraftFusedLayout L{};
+  L.pitch = ((int64_t)V + 7) / 8 * 8;  // 16-byte aligned rows
+  L.part = 0;
+  L.err = align_up(lmhead_part_bytes(R, V), 256);
+  L.logits = align_up(L.err + sizeof(int), 256);
+  L.total = align_up(L.logits + (size_t)R * (size_t)L.pitch * 2, 256);
+  return L;
+}
+
+constexpr int kDraftFusedMaxK = 32;
+
+}  // namespace
+
+extern "C" size_t spec_draft_fused_workspace_size(int32_t R, int32_t V, int32_t k) {
+  if (R < 1 || V < 1 || k < 1 || k > kDraftFusedMaxK || V > SPEC_MAX_VOCAB) return 0;
+  return draft_fused_layout(R, V).total;
+}
+
+extern "C" int spec_draft_topk_fused_lmhead(const void* features, const void* lm_head_w,
+                                            int32_t d, int32_t R, int32_t V, int32_t k,
+                                            float temperature, void* out_logits,
+                                            int64_t logits_pitch, int32_t* out_tokens,
+                                            float* out_probs, int32_t* out_status,
+                                            void* workspace, size_t workspace_bytes,
+                                            spec_stream_t stream) {
+  if (R < 0 || V < 1 || d < 1 || k < 1 || k > kDraftFusedMaxK || k > V) return SPEC_ERR_INVALID_ARG;
+  if (V > SPEC_MAX_VOCAB) return SPEC_ERR_TOO_LARGE;
+  if (!(temperature > 0.0f) || !(temperature <= 3.402823466e38f)) return SPEC_ERR_INVALID_ARG;
+  if (R == 0) return SPEC_OK;
+  if (!features || !lm_head_w || !out_tokens || !out_probs || !workspace) return SPEC_ERR_INVALID_ARG;
+  // the tensor maps need 16-byte aligned bases and rows (d a multiple of 8)
+  if ((reinterpret_cast<uintptr_t>(features) & 15u) || (reinterpret_cast<uintptr_t>(lm_head_w) & 15u) ||
+      d % 8 != 0)
+    return SPEC_ERR_MISALIGNED;
+  if (out_logits) {
+    if (logits_pitch < V) return SPEC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out_logits) & 15u) || (logits_pitch * 2) % 16 != 0)
+      return SPEC_ERR_MISALIGNED;
+  }
+  const DraftFusedLayout L = draft_fused_layout(R, V);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws + L.err);
+  void* logits = out_logits ? out_logits : static_cast<void*>(ws + L.logits);
+  const int64_t pitch = out_logits ? logits_pitch : L.pitch;
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_lmhead_logits(features, lm_head_w, R, V, d, logits, pitch, ws + L.part, err, s) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return draft_topk_impl(logits, SPEC_BF16, R, V, pitch, k, temperature, out_tokens, out_probs,
+                         out_status, err, stream);
 }

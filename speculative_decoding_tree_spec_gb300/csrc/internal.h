@@ -130,6 +130,10 @@ int device_sm_count();
 // launch of the GEMM + statistics kernel and of the combine kernel that writes the
 // row statistics of the M target rows.
 size_t lmhead_part_bytes(int M, int V);
+// The LM-head GEMM alone: bf16 logits F W^T into p (rows of pitch elements), no row
+// statistics (the draft-side top-k ranks the rows itself).
+cudaError_t launch_lmhead_logits(const void* features, const void* weight, int M, int V, int K,
+                                 void* p, int64_t pitch, void* part, int* err, cudaStream_t s);
 cudaError_t launch_lmhead(const void* features, const void* weight, int M, int V, int K,
                           float temperature, void* p, int64_t pitch, void* part, int* err,
                           spec_row_stats* stats, unsigned long long* counters, cudaStream_t s);

@@ -463,4 +463,38 @@ cudaError_t launch_lmhead(const void* features, const void* weight, int M, int V
   return cudaGetLastError();
 }
 
+cudaError_t launch_lmhead_logits(const void* features, const void* weight, int M, int V, int K,
+                                 void* p, int64_t pitch, void* part, int* err, cudaStream_t s) {
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, features, M, K, BM) || !make_map(&tmB, weight, V, K, BN))
+    return cudaErrorInvalidValue;
+  LmJob job{};
+  job.M = M;
+  job.V = V;
+  job.K = K;
+  job.m_tiles = (M + BM - 1) / BM;
+  job.n_tiles = (V + BN - 1) / BN;
+  job.c = 0.f;  // no sums: the caller ranks the written rows itself
+  job.p = static_cast<uint16_t*>(p);
+  job.pitch = pitch;
+  job.part = static_cast<TilePart*>(part);
+  job.err = err;
+  job.wait_limit_ns = 2000000000ull;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kLmSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const int tiles = job.m_tiles * job.n_tiles;
+  int grid = device_sm_count();
+  if (grid > tiles) grid = tiles;
+  lmhead_kernel<<<grid, kLmThreads, kLmSmem, s>>>(tmA, tmB, job);
+  return cudaGetLastError();
+}
+
 }  // namespace svk

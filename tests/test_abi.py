@@ -193,3 +193,24 @@ def test_draft_topk_validation(L):
     assert f(FAKE, 1, 4, 100, 100, 10, 1.0, FAKE, FAKE, None, None) == -3  # 200-byte pitch
     assert f(FAKE, 3, 4, 100, 104, 10, 1.0, FAKE, FAKE, None, None) == -2  # dtype
     assert f(None, 1, 4, 100, 104, 10, 1.0, FAKE, FAKE, None, None) == -1
+
+
+def test_draft_fused_validation(L):
+    f = L.spec_draft_topk_fused_lmhead
+    ws = L.spec_draft_fused_workspace_size(4, 1000, 10)
+    assert ws > 0 and L.spec_draft_fused_workspace_size(4, 1000, 33) == 0
+    ok = lambda **kw: dict(dict(feat=FAKE, w=FAKE, d=64, R=4, V=1000, k=10, T=1.0, lg=None, pitch=0,
+                                tok=FAKE, pr=FAKE, st=None, ws=FAKE, wsb=ws), **kw)
+    call = lambda a: f(a["feat"], a["w"], a["d"], a["R"], a["V"], a["k"], a["T"], a["lg"],
+                       a["pitch"], a["tok"], a["pr"], a["st"], a["ws"], a["wsb"], None)
+    assert call(ok(R=0)) == 0
+    assert call(ok(k=0)) == -1
+    assert call(ok(k=33)) == -1
+    assert call(ok(T=0.0)) == -1
+    assert call(ok(d=60)) == -3          # rows of the tensor maps must be 16-byte multiples
+    assert call(ok(feat=FAKE + 8)) == -3
+    assert call(ok(lg=FAKE, pitch=999)) == -1
+    assert call(ok(lg=FAKE, pitch=1001)) == -3
+    assert call(ok(wsb=ws - 1)) == -4
+    assert call(ok(ws=FAKE + 128)) == -4
+    assert call(ok(w=None)) == -1

@@ -66,6 +66,10 @@ def parse_args():
     ap.add_argument("--fused", action="store_true",
                     help="with --op draft: the draft LM head + top-k in one call (features x "
                          "weight on the tensor cores, then the ranking kernel)")
+    ap.add_argument("--per-request", action="store_true",
+                    help="per-request sampling parameters: the trees cycle through greedy, the "
+                         "workload's own setting, top-k 50 at T=1 and top-p 0.8 at T=0.5 "
+                         "(spec_verify_tree_per_request); reported as its own line")
     ap.add_argument("--visited-only", action="store_true",
                     help="the visited-rows-only schedule (no dense pass); reported as its own "
                          "line, not the dense schedule's number")
@@ -310,8 +314,16 @@ def run_ours(args):
     tok = torch.as_tensor(inp["tokens"], device=dev)
     par = torch.as_tensor(inp["parents"], device=dev)
     flags = binding.SPEC_FLAG_VISITED_ONLY if args.visited_only else 0
+    per_request = None
+    if args.per_request:
+        mix = [(0.0, 0, 1.0), (w.temperature, w.top_k, w.top_p), (1.0, 50, 1.0), (0.5, 0, 0.8)]
+        per_request = (
+            torch.tensor([mix[b % 4][0] for b in range(w.B)], dtype=torch.float32, device=dev),
+            torch.tensor([mix[b % 4][1] for b in range(w.B)], dtype=torch.int32, device=dev),
+            torch.tensor([mix[b % 4][2] for b in range(w.B)], dtype=torch.float32, device=dev))
     call = binding.PreparedVerify(inp["p"], inp["q"], tok, par, inp["max_depth"], w.temperature,
-                                  w.top_k, w.top_p, seed=seed, offset=0, flags=flags)
+                                  w.top_k, w.top_p, seed=seed, offset=0, flags=flags,
+                                  per_request=per_request)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         call()
@@ -364,7 +376,8 @@ def run_ours(args):
                     "avg_launch_ms": walk_ms}
     else:
         achieved = counters["dense_bytes"] / (row_avg_ms / 1e3) / 1e9
-        traffic, traffic_state = profiled_traffic(w.name)
+        # the committed capture is of the one-setting workload
+        traffic, traffic_state = (None, None) if args.per_request else profiled_traffic(w.name)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": traffic,
                     "kernel": "row_pass_kernel (dense row pass)",
@@ -386,6 +399,9 @@ def run_ours(args):
                    "rng_offset": "fixed per step",
                    "schedule": ("visited rows only (no dense pass)" if args.visited_only
                                 else "dense pass over every row"),
+                   "sampling": ("per request: trees cycle through greedy, the workload's "
+                                "setting, top-k 50 at T=1, top-p 0.8 at T=0.5"
+                                if args.per_request else "one setting for every tree"),
                    "l2": f"inputs {2 * w.B * w.N * w.V * (2 if w.dtype == 'bf16' else 4) / 1e9:.2f}"
                          " GB per step, larger than L2; no flush",
                    "parallelism": f"weak: {world} rank(s) x {w.B} trees"},
@@ -397,7 +413,7 @@ def run_ours(args):
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
 
-    if not args.no_e2e:
+    if not args.no_e2e and not args.per_request:
         result["e2e"] = run_e2e(args, w, inp, dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_cpu_baseline(args, w, inp)

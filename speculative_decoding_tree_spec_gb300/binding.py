@@ -551,7 +551,11 @@ class PreparedVerify:
     allocated once), for loops that call the same verify step many times."""
 
     def __init__(self, p, q, draft_tokens, parent_idx, max_depth, temperature, top_k=0,
-                 top_p=1.0, seed=0, offset=0, flags=0, batch_broadcast=False, stream=None):
+                 top_p=1.0, seed=0, offset=0, flags=0, batch_broadcast=False, stream=None,
+                 per_request=None):
+        """per_request: optional (temperature [B] f32, top_k [B] i32 or None, top_p [B]
+        f32 or None) device tensors -- spec_verify_tree_per_request then replaces the
+        scalar temperature / top_k / top_p."""
         B, N = draft_tokens.shape
         V = p.shape[-1]
         dev = p.device
@@ -569,7 +573,21 @@ class PreparedVerify:
         self.counters = torch.zeros(8, dtype=torch.int64, device=dev)
         ws_bytes = int(lib().spec_verify_workspace_size(B, N, V, dt))
         self.workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-        self._keep = (p, q, draft_tokens, parent_idx)
+        self._keep = (p, q, draft_tokens, parent_idx, per_request)
+        if per_request is not None:
+            T_r, k_r, p_r = per_request
+            self._fn = lib().spec_verify_tree_per_request
+            self._args = [
+                p.data_ptr(), q.data_ptr(), dt, B, N, V, pitch, bstride, draft_tokens.data_ptr(),
+                parent_idx.data_ptr(), int(max_depth), T_r.data_ptr(),
+                None if k_r is None else k_r.data_ptr(), None if p_r is None else p_r.data_ptr(),
+                int(flags), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                self.out["accept_len"].data_ptr(), self.out["tokens"].data_ptr(),
+                self.out["path"].data_ptr(), None, self.out["status"].data_ptr(), None,
+                self.workspace.data_ptr(), self.workspace.numel(), _stream_ptr(stream)]
+            self._counter_args = list(self._args)
+            self._counter_args[22] = self.counters.data_ptr()
+            return
         self._fn = lib().spec_verify_tree_phases
         self._args = [
             p.data_ptr(), None if q is None else q.data_ptr(), dt, B, N, V, pitch, bstride,

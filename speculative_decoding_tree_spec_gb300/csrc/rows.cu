@@ -130,8 +130,15 @@ template <> struct Cand<float> {
 // Dynamic shared memory: the ring, its full / empty barriers, the candidate
 // regions, and the selection scratch (histogram, bin weights, ties; or the sort
 // keys of an fp32 window).
-constexpr size_t kRingBytes = (size_t)kRingStages * kStageBytes;
-constexpr size_t kBarBytes = (size_t)kRingStages * 16;
+// The streaming modes (0, 1) need no candidate regions or selection scratch, so their
+// ring runs deeper (more copies in flight) in the same shared memory.
+constexpr int kRingStagesStream = 6;
+template <int MODE>
+__host__ __device__ constexpr int ring_stages() { return MODE == 2 ? kRingStages : kRingStagesStream; }
+template <int MODE>
+__host__ __device__ constexpr size_t ring_bytes() { return (size_t)ring_stages<MODE>() * kStageBytes; }
+template <int MODE>
+__host__ __device__ constexpr size_t bar_bytes() { return (size_t)ring_stages<MODE>() * 16; }
 constexpr size_t kScratchBytes = (size_t)kHistBins * 12 + (size_t)kTieCap * 4 > (size_t)kSortCap * 8
                                      ? (size_t)kHistBins * 12 + (size_t)kTieCap * 4
                                      : (size_t)kSortCap * 8;
@@ -139,9 +146,9 @@ template <typename T>
 __host__ __device__ constexpr size_t cand_bytes() {
   return (size_t)Cand<T>::kCap * sizeof(typename Cand<T>::entry_t);
 }
-template <typename T>
+template <typename T, int MODE>
 __host__ __device__ constexpr size_t row_dyn_smem() {
-  return kRingBytes + kBarBytes + cand_bytes<T>() + kScratchBytes;
+  return ring_bytes<MODE>() + bar_bytes<MODE>() + (MODE == 2 ? cand_bytes<T>() + kScratchBytes : 0);
 }
 
 // 16-bit order key of the bf16 logit with raw bits b.
@@ -231,17 +238,19 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kernel(RowJob job) {
   constexpr int E = Elt<T>::kPerUnit;
   constexpr int U = kRingUnits;
-  constexpr int S = kRingStages;
+  constexpr int S = ring_stages<MODE>();
   constexpr int CAP = Cand<T>::kCap;
   constexpr int CAPW = CAP / NW;  // candidate region of one warp
   using entry_t = typename Cand<T>::entry_t;
   __shared__ RowShared sh;
   extern __shared__ __align__(128) unsigned char dyn[];
   uint4* ring = reinterpret_cast<uint4*>(dyn);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(dyn + kRingBytes);
+  // (modes 0 and 1 allocate no candidate regions or scratch: those pointers are formed
+  // but never used there)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(dyn + ring_bytes<MODE>());
   uint64_t* empty_bar = full_bar + S;
-  entry_t* cand = reinterpret_cast<entry_t*>(dyn + kRingBytes + kBarBytes);
-  unsigned char* scratch = dyn + kRingBytes + kBarBytes + cand_bytes<T>();
+  entry_t* cand = reinterpret_cast<entry_t*>(dyn + ring_bytes<MODE>() + bar_bytes<MODE>());
+  unsigned char* scratch = dyn + ring_bytes<MODE>() + bar_bytes<MODE>() + cand_bytes<T>();
   unsigned* hist = reinterpret_cast<unsigned*>(scratch);
   unsigned long long* wbin = reinterpret_cast<unsigned long long*>(scratch + (size_t)kHistBins * 4);
   unsigned* ties = reinterpret_cast<unsigned*>(scratch + (size_t)kHistBins * 12);
@@ -901,7 +910,7 @@ __global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kerne
 
 template <typename T, int MODE>
 cudaError_t launch_mode(const RowJob& job, int num_rows, cudaStream_t s) {
-  const size_t dyn = row_dyn_smem<T>();
+  const size_t dyn = row_dyn_smem<T, MODE>();
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -130,11 +130,15 @@ template <> struct Cand<float> {
 // Dynamic shared memory: the ring, its full / empty barriers, the candidate
 // regions, and the selection scratch (histogram, bin weights, ties; or the sort
 // keys of an fp32 window).
-// The streaming modes (0, 1) need no candidate regions or selection scratch, so their
-// ring runs deeper (more copies in flight) in the same shared memory.
-constexpr int kRingStagesStream = 6;
+// The streaming modes (0, 1) need no candidate regions or selection scratch: their
+// blocks are small enough for 4 per SM (3 ring stages each, 56 registers), twice the
+// warps of the cutting mode's 2 blocks to cover the latency of the stages in flight.
+constexpr int kRingStagesStream = 3;
+constexpr int kRowBlocksStream = 4;  // resident blocks per SM in the streaming modes
 template <int MODE>
 __host__ __device__ constexpr int ring_stages() { return MODE == 2 ? kRingStages : kRingStagesStream; }
+template <int MODE>
+__host__ __device__ constexpr int row_blocks() { return MODE == 2 ? kRowBlocksPerSm : kRowBlocksStream; }
 template <int MODE>
 __host__ __device__ constexpr size_t ring_bytes() { return (size_t)ring_stages<MODE>() * kStageBytes; }
 template <int MODE>
@@ -235,7 +239,7 @@ __device__ __forceinline__ uint32_t window_slot(int bit, int& k, int& e) {
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kBlockThreads, kRowBlocksPerSm) row_pass_kernel(RowJob job) {
+__global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_kernel(RowJob job) {
   constexpr int E = Elt<T>::kPerUnit;
   constexpr int U = kRingUnits;
   constexpr int S = ring_stages<MODE>();
@@ -921,7 +925,7 @@ cudaError_t launch_mode(const RowJob& job, int num_rows, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  int grid = device_sm_count() * kRowBlocksPerSm;  // persistent blocks
+  int grid = device_sm_count() * row_blocks<MODE>();  // persistent blocks
   if (grid > num_rows) grid = num_rows;
   if (grid < 1) grid = 1;
   row_pass_kernel<T, MODE><<<grid, kBlockThreads, dyn, s>>>(job);

@@ -1467,12 +1467,16 @@ __device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const vo
   int bad[2] = {0, 0};
   if (threadIdx.x < 2) sh.st_bad[threadIdx.x] = 0;
   __syncthreads();
-  for (int u = ua + (int)threadIdx.x; u < ub; u += CT) {
+  // the slices stream through the ring; a thread meets its units in increasing order,
+  // so the first index of a strictly larger maximum is its first occurrence
+  stream_slice<T>(rows, nrows, V, ua, ub, sh, [&](int u, bool valid, const uint4& raw0,
+                                                   const uint4& raw1) {
+    if (!valid) return;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;
       float z[E];
-      load_unit<T>(rows[r], V, u, z);
+      Elt<T>::unpack(r ? raw1 : raw0, z);
       float um = z[0];
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -1499,7 +1503,7 @@ __device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const vo
         ks[r].add(part);
       }
     }
-  }
+  });
   for (int r = 0; r < nrows; ++r) {
     const float wm = warp_max(tm[r]);
     FF sv = ks[r].ff();

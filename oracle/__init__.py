@@ -143,6 +143,14 @@ def filter_rows(rows, temperature: float, top_k: int, top_p: float, want_probs: 
     return probs, list(infos)
 
 
+NEAR_BITS = {"p_cut": 1, "q_cut": 2, "accept": 4, "draw": 8}
+
+
+def near_reasons(bits: int):
+    """Names of the near-boundary decisions in one tree's near bits."""
+    return [k for k, v in NEAR_BITS.items() if int(bits) & v]
+
+
 def verify_tree(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
                 temperature: float, top_k: int, top_p: float, seed: int, offset: int = 0,
                 u_accept=None, u_final=None, want_final_dist: bool = False,
@@ -154,6 +162,9 @@ def verify_tree(logits_p, logits_q, draft_tokens, parent_idx, max_depth: int,
     Tree b draws its uniforms as batch index batch_index + b.
     Returns a dict of numpy arrays: accept_len [B], tokens [B, D+1], path [B, D+1],
     alpha [B, N], status [B], near [B] and optionally final_dist [B, V].
+    near[b] marks the decisions of tree b that fell within 1e-6 of their boundary,
+    where rounding order alone could flip them: bit NEAR_BITS["p_cut"] (a p row's
+    top-p cut), "q_cut", "accept" (|r - alpha|) and "draw" (the final inverse CDF).
     """
     p, dt = _as_logits(logits_p)
     q, dq = _as_logits(logits_q)

@@ -285,6 +285,13 @@ static void fail_tree(const walk_args* a, int b, int status) {
   if (a->out_status) a->out_status[b] = status;
 }
 
+/* Which decision of a tree fell within ORACLE_NEAR of its boundary (bits of
+   out_near): a p row's or a q row's top-p cut, an accept test, the final draw. */
+#define NEAR_P_CUT 1
+#define NEAR_Q_CUT 2
+#define NEAR_ACCEPT 4
+#define NEAR_DRAW 8
+
 /* Inverse CDF in index order: the smallest i with C_i >= r * C_V. */
 static int inverse_cdf(const double* P, int V, double r, int* near) {
   double total = 0.0;
@@ -298,13 +305,13 @@ static int inverse_cdf(const double* P, int V, double r, int* near) {
     if (P[i] > 0.0 && cum >= target) {
       pick = i;
       if (fabs(target - prev) < ORACLE_NEAR * total || fabs(target - cum) < ORACLE_NEAR * total)
-        *near = 1;
+        *near |= NEAR_DRAW;
       break;
     }
   }
   if (pick < 0) /* r == 1 and rounding: take the last token with mass */
     for (int i = V - 1; i >= 0; --i)
-      if (P[i] > 0.0) { pick = i; *near = 1; break; }
+      if (P[i] > 0.0) { pick = i; *near |= NEAR_DRAW; break; }
   return pick;
 }
 
@@ -353,7 +360,7 @@ static void walk_one_tree(const walk_args* a, int b) {
       fail_tree(a, b, ORACLE_ROW_NONFINITE);
       return;
     }
-    near |= pi.near;
+    if (pi.near) near |= NEAR_P_CUT;
     int has_child = 0;
     for (int c = u + 1; c < N; ++c)
       if (par[c] == u) { has_child = 1; break; }
@@ -388,7 +395,7 @@ static void walk_one_tree(const walk_args* a, int b) {
         fail_tree(a, b, ORACLE_ROW_NONFINITE);
         return;
       }
-      near |= qi.near;
+      if (qi.near) near |= NEAR_Q_CUT;
     }
 
     int next = -1;
@@ -405,7 +412,7 @@ static void walk_one_tree(const walk_args* a, int b) {
       double r = a->u_accept ? a->u_accept[(int64_t)b * N + c]
                              : oracle_uniform(a->seed, a->offset, a->rng_b0 + b, c, 0);
       if (a->out_alpha) a->out_alpha[(int64_t)b * N + c] = alpha;
-      if (fabs(r - alpha) < ORACLE_NEAR) near = 1;
+      if (fabs(r - alpha) < ORACLE_NEAR) near |= NEAR_ACCEPT;
       if (r <= alpha) {
         next = c;
       } else {
@@ -469,7 +476,8 @@ static void* walk_slice_main(void* arg) {
  * u_accept / u_final, when non-NULL,
  * replace the Philox uniforms ([B, N] each, indexed by the tested child /
  * the node of the final draw).  out_alpha [B, N] (NaN where untested),
- * out_near [B], out_final_dist [B, V] are optional.  Returns 0.
+ * out_near [B] (the NEAR_* bits of the decisions that fell within ORACLE_NEAR of
+ * their boundary, 0 if none), out_final_dist [B, V] are optional.  Returns 0.
  */
 int oracle_verify_tree(const void* logits_p, const void* logits_q, int dtype, int B, int N, int V,
                        int64_t row_pitch, int64_t batch_stride, const int32_t* draft_tokens,

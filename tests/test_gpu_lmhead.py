@@ -1,6 +1,8 @@
 """The fused LM head (spec_verify_tree_fused_lmhead): the target logits it computes on
 the tensor cores against torch.matmul with fp32 accumulation, rounded to bf16; and the
 verify outputs it gives against the oracle run on those same logits."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -94,23 +96,32 @@ def test_fused_equals_verify_on_the_same_logits():
 
 def test_fused_full_size_sampled():
     """The full workload (32 trees x 60 nodes, d 4096, V 128256): sampled logit rows
-    against matmul, and sampled trees against the oracle."""
+    against matmul, and every tree against the oracle.  These logits are flat (std
+    1.28 at T = 0.8: near the top-p cut a token carries about 4e-6 of the mass), so
+    many trees have a cut or a draw within the oracle's 1e-6 margin and are left
+    out (each logged with its reason); batches of fresh features run until at least
+    8 trees have been compared, and every compared tree must match."""
     w = BASE
-    inp = _inputs(w, 20261202)
-    out = _run(w, inp, seed=5)
-    rows = torch.arange(0, w.B * w.N, 97, device=DEV)
-    _check_logits(out["p"], inp["features"], inp["weight"], rows)
-    gpu = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in out.items() if k != "p"}
-    oinp = {"p": out["p"], "q": inp["q"], "tokens": inp["tokens"], "parents": inp["parents"],
-            "max_depth": inp["max_depth"]}
-    # the verify step on these logits: identical to spec_verify_tree on the same rows
-    plain = binding.verify_tree(out["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
-                                inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=5)
-    torch.cuda.synchronize()
-    for k in ("accept_len", "tokens", "path", "status"):
-        np.testing.assert_array_equal(gpu[k], plain[k].cpu().numpy(), err_msg=k)
-    # these logits are flat (std 1.28 at T = 0.8: near the top-p cut a token carries
-    # about 4e-6 of the mass), so most trees have a cut or a draw within the oracle's
-    # 1e-6 margin and are excluded; the trees that remain must match
-    sel, outs = run_oracle(w, oinp, trees=list(range(0, w.B, 4)), seed=5)
-    compare(w, gpu, sel, outs)
+    compared = 0
+    for seed in (20261202, 20261203, 20261204, 20261205):
+        inp = _inputs(w, seed)
+        out = _run(w, inp, seed=5)
+        rows = torch.arange(seed % 97, w.B * w.N, 97, device=DEV)
+        _check_logits(out["p"], inp["features"], inp["weight"], rows)
+        gpu = {k: (v.cpu().numpy() if torch.is_tensor(v) else v)
+               for k, v in out.items() if k != "p"}
+        oinp = {"p": out["p"], "q": inp["q"], "tokens": inp["tokens"],
+                "parents": inp["parents"], "max_depth": inp["max_depth"]}
+        # the verify step on these logits: identical to spec_verify_tree on the same rows
+        plain = binding.verify_tree(out["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
+                                    inp["max_depth"], w.temperature, w.top_k, w.top_p, seed=5)
+        torch.cuda.synchronize()
+        for k in ("accept_len", "tokens", "path", "status"):
+            np.testing.assert_array_equal(gpu[k], plain[k].cpu().numpy(), err_msg=k)
+        sel, outs = run_oracle(w, oinp, seed=5, threads=max(1, min(16, os.cpu_count() or 1)))
+        n, ex, _ = compare(w, gpu, sel, outs)
+        compared += n
+        del inp, out, plain
+        if compared >= 8:
+            break
+    assert compared >= 8, compared

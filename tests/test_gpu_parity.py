@@ -3,6 +3,8 @@ same seeded inputs.  Token ids, accepted lengths, paths, argmax and cut indices
 must match exactly; probabilities within 1e-5 relative for fp32 logits and 2e-3
 for bf16 logits.  Trees / rows the oracle flags as within 1e-6 of a decision
 boundary are excluded from the exact comparison and counted."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -199,6 +201,26 @@ def test_eagle10_v32000(T):
 ], ids=["c3-reduced", "c4-reduced", "c3-f32", "c4-greedy", "ragged-topk-topp", "f32-plain"])
 def test_random_trees(w):
     _parity(w, seed=21)
+
+
+# --- the benchmarked workloads at their own sizes: the launch geometry the bench times
+# (the walk's cluster size follows B: 4 CTAs per tree at B = 64, one at B = 256) -------
+
+HOST_THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.mark.parametrize("name,seed,min_compared", [
+    ("tree60_b64_v128256", 20261202, 32), ("tree60_b64_v128256", 5, 32),
+    ("tree26_b256_v152064", 20261202, 128), ("tree26_b256_v152064", 77, 128)])
+def test_benchmarked_workload_every_tree(name, seed, min_compared):
+    w = W[name]
+    inp = gpu_inputs(w, seed)
+    gpu = run_gpu(w, inp, seed=seed + 1)
+    sel, outs = run_oracle(w, inp, seed=seed + 1, threads=HOST_THREADS)
+    n, ex, err = compare(w, gpu, sel, outs)
+    print(f"{name} seed {seed}: {n} trees compared, {ex} excluded, max alpha error {err:.2e}, "
+          f"cut rows through the full-row selection {gpu['counters']['fallback_rows']}")
+    assert len(sel) == w.B and n >= min_compared, (n, ex)
 
 
 def test_exact_select_flag_gives_identical_outputs():

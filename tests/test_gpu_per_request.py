@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from parity_helpers import ALPHA_RTOL, gpu_inputs
+from parity_helpers import ALPHA_RTOL, gpu_inputs, log_exclusions
 from speculative_decoding_tree_spec_gb300 import binding
 from speculative_decoding_tree_spec_gb300 import workloads as wl
 
@@ -40,11 +40,13 @@ def _check_vs_oracle(w, inp, gpu, T, k, p, seed=9):
                                          T.cpu().numpy(), k.cpu().numpy(), p.cpu().numpy(),
                                          seed=seed)
     compared = 0
+    skipped = []
     for b, o in enumerate(ref):
         if o is None:
             assert gpu["status"][b] == 2 and gpu["accept_len"][b] == -1, b
             continue
         if o["near"][0]:
+            skipped.append((b, oracle.near_reasons(o["near"][0])))
             continue
         compared += 1
         assert gpu["status"][b] == o["status"][0], b
@@ -57,6 +59,7 @@ def _check_vs_oracle(w, inp, gpu, T, k, p, seed=9):
         err = np.abs(ga[m] - oa[m]) / np.maximum(np.abs(oa[m]), 1e-30)
         err = np.where(oa[m] == 0, np.abs(ga[m]), err)
         assert (err <= ALPHA_RTOL[w.dtype]).all(), (b, err.max() if err.size else 0)
+    log_exclusions(w, skipped)
     return compared
 
 

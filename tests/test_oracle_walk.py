@@ -222,3 +222,40 @@ def test_non_finite_row_on_the_walk_is_reported():
     # greedy never reads q
     out = oracle.verify_tree(p, q, tokens, parents, 2, 0.0, 0, 1.0, seed=0)
     assert out["status"][0] == 0
+
+
+def test_near_bits_name_the_decision_at_its_boundary():
+    """The near flag says which decision sat within 1e-6 of its threshold: an accept
+    test with r equal to alpha, a final draw with r on a CDF step, a top-p cut whose
+    cumulative mass lands on top_p."""
+    V, T = 4, 1.0
+    # root with one child; p uniform, q concentrated so alpha of token 0 is 1/4 / 1/2
+    p = np.zeros((1, 2, V), np.float32)
+    q = np.zeros((1, 2, V), np.float32)
+    q[0, 0] = np.log(np.array([2.0, 1.0, 0.5, 0.5], np.float32))
+    tok = np.array([[0, 0]], np.int32)
+    par = np.array([[-1, 0]], np.int32)
+    Q = np.array([2.0, 1.0, 0.5, 0.5]) / 4.0
+    alpha = 0.25 / Q[0]
+    ua = np.array([[0.0, alpha]], np.float64)
+    uf = np.full((1, 2), 0.37, np.float64)
+    out = oracle.verify_tree(p, q, tok, par, 1, T, 0, 1.0, seed=1, u_accept=ua, u_final=uf)
+    assert oracle.near_reasons(out["near"][0]) == ["accept"]
+    # rejected (r above alpha), then the draw from norm(max(0, p - q)) lands on a step
+    resid = np.maximum(0.0, 0.25 - Q)
+    cdf = np.cumsum(resid) / resid.sum()
+    ua = np.array([[0.0, 0.9]], np.float64)
+    uf = np.array([[cdf[2], 0.0]], np.float64)
+    out = oracle.verify_tree(p, q, tok, par, 1, T, 0, 1.0, seed=1, u_accept=ua, u_final=uf)
+    assert oracle.near_reasons(out["near"][0]) == ["draw"]
+    assert out["tokens"][0, 0] == 2
+    # a leaf root whose top-p threshold equals a cumulative mass: p-row cut only
+    p1 = np.log(np.array([[[4.0, 2.0, 1.0, 1.0]]], np.float32))
+    out = oracle.verify_tree(p1, p1, np.zeros((1, 1), np.int32), np.full((1, 1), -1, np.int32),
+                             0, T, 0, 0.75, seed=1, u_final=np.array([[0.3]]))
+    assert oracle.near_reasons(out["near"][0]) == ["p_cut"]
+    # a node with children whose q row has that cut too: both cut bits
+    out = oracle.verify_tree(np.concatenate([p1, p1], 1), np.concatenate([p1, p1], 1),
+                             tok, par, 1, T, 0, 0.75, seed=1, u_accept=np.array([[0.0, 0.5]]),
+                             u_final=np.full((1, 2), 0.3))
+    assert {"p_cut", "q_cut"} <= set(oracle.near_reasons(out["near"][0]))

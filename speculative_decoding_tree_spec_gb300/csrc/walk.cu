@@ -516,6 +516,10 @@ struct CShared {
   unsigned kp_n;    // this CTA's kept tokens of p (kept-set mode)
   unsigned long long ured[CW];
   int kp_tok;
+  // top-k route: per row, the list threshold (an order key) and the selection digits
+  uint32_t tk_thr[2];
+  int tk_d1[2];
+  unsigned tk_above[2];
 };
 
 struct BSync {
@@ -1576,6 +1580,407 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// bf16 rows under top-k (1 <= k <= kTopkList).  The window's key histogram cannot
+// span a window that crosses zero (bf16 keys are dense there), and a window of
+// thousands of tokens overflows the lists; but only the row's k largest tokens
+// matter.  So each CTA keeps the list of its slice's tokens at or above a
+// threshold that starts at m - delta_z and, whenever the list fills, rises to the
+// k-th largest 16-bit key the list holds: the CTA's own k largest tokens never
+// fall below it.  The union of the CTAs' lists holds the row's k largest tokens;
+// sorted (logit desc, index asc) they give the cut by the dense row pass's rule
+// (top-k, then the top-p crossing within it), and p's kept set is in the lists.
+// ---------------------------------------------------------------------------
+constexpr int kTopkList = 128;  // largest k this route takes
+constexpr int kTkSort = 1024;   // merged list entries it sorts, per row
+constexpr int kTkRetry = 8;     // threshold raises one round of loads may take
+
+// Its buffers inside the cut's shared memory: two sets of this CTA's lists
+// [2 sets][2 rows][kCandCTA] (the sets alternate from node to node, so a list the
+// other CTAs read is rewritten only after an exchange that each of them reaches
+// after reading it), the sort buffers [2][kTkSort], the digit counts [2][256].
+__device__ __forceinline__ uint64_t* tk_list(unsigned char* smem, uint32_t set, int r) {
+  return reinterpret_cast<uint64_t*>(smem) + ((size_t)(set & 1u) * 2 + r) * kCandCTA;
+}
+__device__ __forceinline__ uint64_t* tk_sortb(unsigned char* smem, int r) {
+  return reinterpret_cast<uint64_t*>(smem) + 4 * kCandCTA + (size_t)r * kTkSort;
+}
+__device__ __forceinline__ unsigned* tk_hist(unsigned char* smem, int r) {
+  return reinterpret_cast<unsigned*>(reinterpret_cast<uint64_t*>(smem) + 4 * kCandCTA +
+                                     2 * kTkSort) + r * 256;
+}
+constexpr size_t kTkSmemBytes = (4 * (size_t)kCandCTA + 2 * (size_t)kTkSort) * 8 + 2 * 256 * 4;
+
+// One warp: the digit (0..255) at which the counts, taken from digit 255 down,
+// reach `need` (1 <= need <= their total); `above` = the count of the digits above it.
+__device__ void tk_digit(const unsigned* hist, unsigned need, int& digit, unsigned& above) {
+  const int lane = threadIdx.x & 31;
+  unsigned s = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) s += hist[255 - (8 * lane + t)];
+  unsigned incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const unsigned base = incl - s;
+  int d = INT_MAX;
+  unsigned ab = 0;
+  if (base < need && need <= incl) {
+    unsigned run = base;
+    for (int t = 0; t < 8; ++t) {
+      const unsigned h = hist[255 - (8 * lane + t)];
+      if (run + h >= need) { d = 255 - (8 * lane + t); ab = run; break; }
+      run += h;
+    }
+  }
+  const unsigned who = __ballot_sync(kFull, d != INT_MAX);
+  const int src = who ? __ffs(who) - 1 : 0;
+  digit = __shfl_sync(kFull, d, src);
+  above = __shfl_sync(kFull, ab, src);
+}
+
+// Raises row r's threshold to the K-th largest 16-bit key among this CTA's n list
+// entries (K <= n <= kCandCTA) and keeps the entries at or above it (at least K).
+// Every thread calls it.
+__device__ __noinline__ void tk_compact(uint64_t* list, unsigned n, unsigned K, unsigned* hist, CShared& sh,
+                           int r) {
+  constexpr int PER = kCandCTA / CT;
+  uint64_t mine[PER];
+#pragma unroll
+  for (int t = 0; t < PER; ++t) {
+    const unsigned i = threadIdx.x + t * CT;
+    mine[t] = i < n ? list[i] : 0ull;
+  }
+  for (int i = threadIdx.x; i < 256; i += CT) hist[i] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < PER; ++t)
+    if (threadIdx.x + t * CT < n) atomicAdd(&hist[(unsigned)(mine[t] >> 56)], 1u);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int d;
+    unsigned ab;
+    tk_digit(hist, K, d, ab);
+    if (threadIdx.x == 0) { sh.tk_d1[r] = d; sh.tk_above[r] = ab; }
+  }
+  __syncthreads();
+  const unsigned d1 = (unsigned)sh.tk_d1[r];
+  for (int i = threadIdx.x; i < 256; i += CT) hist[i] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < PER; ++t)
+    if (threadIdx.x + t * CT < n && (unsigned)(mine[t] >> 56) == d1)
+      atomicAdd(&hist[(unsigned)(mine[t] >> 48) & 255u], 1u);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int d;
+    unsigned ab;
+    tk_digit(hist, K - sh.tk_above[r], d, ab);
+    if (threadIdx.x == 0) {
+      sh.tk_thr[r] = key_from16((d1 << 8) | (unsigned)d);
+      sh.ncand[r] = 0u;
+    }
+  }
+  __syncthreads();
+  const uint32_t thr = sh.tk_thr[r];
+  unsigned keep = 0;
+#pragma unroll
+  for (int t = 0; t < PER; ++t)
+    keep += (threadIdx.x + t * CT < n && (uint32_t)(mine[t] >> 32) >= thr) ? 1u : 0u;
+  unsigned pos = warp_reserve(&sh.ncand[r], keep);
+#pragma unroll
+  for (int t = 0; t < PER; ++t)
+    if (threadIdx.x + t * CT < n && (uint32_t)(mine[t] >> 32) >= thr) list[pos++] = mine[t];
+  __syncthreads();
+}
+
+// The pass over units [ua, ub) of one or two rows (loads as in window_collect_fast):
+// tokens whose order key reaches sh.tk_thr[r] go to list[r] (sh.ncand[r] entries).
+// A round whose tokens overflow a list raises the threshold and re-inserts them
+// from registers; a list past half full is compacted between rounds.  fail[r] is
+// set when kTkRetry raises do not make room (ties at one key).
+__device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int ua, int ub,
+                           uint64_t* const (&list)[2], unsigned K, unsigned* const (&hist)[2],
+                           CShared& sh, bool (&fail)[2]) {
+  const int full = V / 8;
+  const int ubf = min(ub, full);
+  const uint4* const r0 = reinterpret_cast<const uint4*>(rows[0]);
+  const uint4* const r1 = reinterpret_cast<const uint4*>(nrows > 1 ? rows[1] : rows[0]);
+  const int nround = (ubf > ua ? (ubf - ua + CT * kWinUnits - 1) / (CT * kWinUnits) : 0) +
+                     (ub > full ? 1 : 0);
+  for (int rd = 0; rd < nround; ++rd) {  // the same rounds in every thread
+    const bool tail = ub > full && rd == nround - 1;
+    const int base = tail ? full : ua + rd * CT * kWinUnits;
+    uint4 raw[2][kWinUnits];
+    if (!tail) {
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const int u = base + h * CT + (int)threadIdx.x;
+        const bool in = u < ubf;
+        raw[0][h] = in ? __ldg(r0 + u)
+                       : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        raw[1][h] = (in && nrows > 1)
+                        ? __ldg(r1 + u)
+                        : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          raw[r][h] = (h == 0 && threadIdx.x == 0 && r < nrows)
+                          ? load_raw<uint16_t>(rows[r], V, full)
+                          : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+    }
+    // members at or above the threshold, inserted; those past the list's end kept
+    // in drop[r][h] (register bits) for after the threshold rises
+    uint32_t drop[2][kWinUnits];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t thr = sh.tk_thr[r];
+      const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(key_value(thr)));
+      uint32_t mb[kWinUnits];
+      unsigned cnt = 0;
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const uint4 v = raw[r][h];
+        uint32_t m = 0;
+        const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)),
+                                         __hmax2(as_bf2(v.z), as_bf2(v.w)));
+        if (r < nrows && !fail[r] && __hge2_mask(a, t2)) {
+          float z[8];
+          Elt<uint16_t>::unpack(v, z);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m |= (order_key(z[e]) >= thr) ? (1u << e) : 0u;
+        }
+        mb[h] = m;
+        drop[r][h] = 0u;
+        cnt += __popc(m);
+      }
+      if (!__any_sync(kFull, cnt != 0u)) continue;
+      unsigned pos = warp_reserve(&sh.ncand[r], cnt);
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        uint32_t bits = mb[h];
+        if (!bits) continue;
+        float z[8];
+        Elt<uint16_t>::unpack(raw[r][h], z);
+        const int u = tail ? full : base + h * CT + (int)threadIdx.x;
+        while (bits) {
+          const int e = __ffs(bits) - 1;
+          bits &= bits - 1u;
+          if (pos < (unsigned)kCandCTA)
+            list[r][pos] = ((uint64_t)order_key(z[e]) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+          else
+            drop[r][h] |= 1u << e;
+          ++pos;
+        }
+      }
+    }
+    // the list sizes, read by every thread between two barriers (the next round's
+    // reservations may not start before all have read them)
+    __syncthreads();
+    const unsigned n_end[2] = {sh.ncand[0], sh.ncand[1]};
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows || fail[r]) continue;
+      unsigned n = n_end[r];
+      if (n <= (unsigned)kCandCTA) {
+        if (n > (unsigned)kCandCTA / 2) tk_compact(list[r], n, K, hist[r], sh, r);
+        continue;
+      }
+      for (int it = 0;; ++it) {
+        if (it == kTkRetry) { fail[r] = true; break; }
+        // the list is full: raise the threshold on what it holds, then re-insert the
+        // round's tokens that did not fit and still reach it
+        tk_compact(list[r], (unsigned)kCandCTA, K, hist[r], sh, r);
+        const uint32_t thr = sh.tk_thr[r];
+        unsigned cnt = 0;
+        // the units are read again (from cache) rather than held in registers
+        auto unit = [&](int h) {
+          const int u = tail ? full : base + h * CT + (int)threadIdx.x;
+          if (tail) return load_raw<uint16_t>(rows[r], V, full);
+          return u < ubf ? __ldg(reinterpret_cast<const uint4*>(rows[r]) + u)
+                         : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        };
+#pragma unroll
+        for (int h = 0; h < kWinUnits; ++h) {
+          uint32_t bits = drop[r][h], keep = 0u;
+          if (bits) {
+            float z[8];
+            Elt<uint16_t>::unpack(unit(h), z);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (((bits >> e) & 1u) && order_key(z[e]) >= thr) keep |= 1u << e;
+          }
+          drop[r][h] = keep;
+          cnt += __popc(keep);
+        }
+        unsigned pos = warp_reserve(&sh.ncand[r], cnt);
+#pragma unroll
+        for (int h = 0; h < kWinUnits; ++h) {
+          uint32_t bits = drop[r][h], left = 0u;
+          if (!bits) continue;
+          float z[8];
+          Elt<uint16_t>::unpack(unit(h), z);
+          const int u = tail ? full : base + h * CT + (int)threadIdx.x;
+          while (bits) {
+            const int e = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            if (pos < (unsigned)kCandCTA)
+              list[r][pos] = ((uint64_t)order_key(z[e]) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+            else
+              left |= 1u << e;
+            ++pos;
+          }
+          drop[r][h] = left;
+        }
+        __syncthreads();
+        n = sh.ncand[r];
+        if (n <= (unsigned)kCandCTA) break;
+      }
+      if (fail[r] && threadIdx.x == 0) sh.ncand[r] = 0u;
+      __syncthreads();
+    }
+  }
+}
+
+// The cut of the p row (and of the q row when with_q) under top-k by the route
+// above; rows it cannot decide go to the exact selection.  p_list receives this
+// CTA's list of p (sh.ncand[0] entries), which holds its slice's part of p's kept
+// set when p_listed.
+__device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const void* qrow,
+                                 bool with_q, spec_row_stats& sp, spec_row_stats& sq, int ua,
+                                 int ub, unsigned char* smem, uint32_t n_visit, CShared& sh,
+                                 int C, uint32_t rank, uint32_t& n_ex, const Samp& smp,
+                                 bool& p_listed, const uint64_t*& p_list) {
+  p_listed = false;
+  const float c = smp.c;
+  const int V = job.V;
+  const int nrows = with_q ? 2 : 1;
+  const unsigned K = (unsigned)smp.top_k;
+  spec_row_stats* st[2] = {&sp, &sq};
+  const void* const rows[2] = {prow, qrow};
+  uint64_t* const list[2] = {tk_list(smem, n_visit, 0), tk_list(smem, n_visit, 1)};
+  unsigned* const hist[2] = {tk_hist(smem, 0), tk_hist(smem, 1)};
+  p_list = list[0];
+  if (threadIdx.x < 2) {
+    const int r = threadIdx.x;
+    sh.ncand[r] = 0u;
+    sh.tk_thr[r] = order_key(st[r]->m - smp.delta_z);
+  }
+  __syncthreads();
+  bool fail[2] = {false, nrows < 2};
+  tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, fail);
+  // every CTA's list sizes (all ones: the row failed somewhere)
+  auto exchange = [&](unsigned (&total)[2], bool (&bad)[2], unsigned (&cnt)[2][kMaxC]) -> bool {
+    uint64_t w = 0;
+    for (int r = 0; r < 2; ++r)
+      w |= (uint64_t)(fail[r] ? 0xffffffffu : sh.ncand[r]) << (32 * r);
+    const SlotRow* sl = cluster_share(&w, 1, sh, C, rank, n_ex);
+    if (!sl) return false;
+    for (int r = 0; r < 2; ++r) {
+      total[r] = 0u;
+      bad[r] = false;
+      for (int q = 0; q < C; ++q) {
+        const unsigned v = (unsigned)(sl[q][0] >> (32 * r));
+        bad[r] |= v == 0xffffffffu;
+        cnt[r][q] = v;
+        total[r] += bad[r] ? 0u : v;
+      }
+    }
+    return true;
+  };
+  unsigned total[2], cnt[2][kMaxC];
+  bool bad[2];
+  if (!exchange(total, bad, cnt)) return false;
+  // a row whose window held fewer than K tokens (its K-th largest lies more than
+  // delta_z below the maximum) is collected again with no floor
+  const bool redo[2] = {!bad[0] && total[0] < K, nrows > 1 && !bad[1] && total[1] < K};
+  if (redo[0] || redo[1]) {
+    if (threadIdx.x < 2 && redo[threadIdx.x]) {
+      sh.ncand[threadIdx.x] = 0u;
+      // the lowest finite key: -inf tokens (and the -inf padding of units past the
+      // slice) never enter a list
+      sh.tk_thr[threadIdx.x] = order_key(-3.402823466e38f);
+    }
+    __syncthreads();
+    bool again[2] = {!redo[0], !redo[1]};  // rows set here are skipped
+    tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, again);
+    for (int r = 0; r < 2; ++r)
+      if (redo[r]) fail[r] = again[r];
+    if (!exchange(total, bad, cnt)) return false;
+  }
+  bool ok[2];
+  for (int r = 0; r < 2; ++r) ok[r] = r < nrows && !bad[r] && total[r] >= K;
+  if ((ok[0] && total[0] > (unsigned)kTkSort) || (ok[1] && total[1] > (unsigned)kTkSort)) {
+    // too many to sort: each CTA keeps its own K largest (the lists were final at
+    // the exchange; they change only now, and are read after the next one)
+    for (int r = 0; r < nrows; ++r)
+      if (ok[r] && sh.ncand[r] > K) tk_compact(list[r], sh.ncand[r], K, hist[r], sh, r);
+    if (!exchange(total, bad, cnt)) return false;
+    for (int r = 0; r < 2; ++r) ok[r] = ok[r] && !bad[r] && total[r] >= K;
+  }
+  unsigned n_pad[2] = {2u, 2u};
+  for (int r = 0; r < 2; ++r) {
+    ok[r] = ok[r] && total[r] <= (unsigned)kTkSort;
+    while (n_pad[r] < total[r]) n_pad[r] <<= 1;
+  }
+  // gather every CTA's list (remote shared memory) into the sort buffers
+  for (int r = 0; r < nrows; ++r) {
+    if (!ok[r]) continue;
+    uint64_t* keys = tk_sortb(smem, r);
+    for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
+      uint64_t v = 0ull;
+      if (i < total[r]) {
+        unsigned off = 0, q = 0;
+        while (q + 1 < (unsigned)C && i >= off + cnt[r][q]) { off += cnt[r][q]; ++q; }
+        v = ld_peer_u64(peer_addr(list[r] + (i - off), q));
+      }
+      keys[i] = v;
+    }
+  }
+  __syncthreads();
+  const unsigned pad_max = max(ok[0] ? n_pad[0] : 0u, ok[1] ? n_pad[1] : 0u);
+  for (unsigned k = 2; k <= pad_max; k <<= 1) {  // bitonic sort, descending
+    for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int r = 0; r < nrows; ++r) {
+        if (!ok[r] || k > n_pad[r]) continue;
+        uint64_t* keys = tk_sortb(smem, r);
+        for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
+          const unsigned ixj = i ^ jj;
+          if (ixj > i) {
+            const uint64_t a = keys[i], b = keys[ixj];
+            const bool swap = ((i & k) == 0) ? (a < b) : (a > b);
+            if (swap) { keys[i] = b; keys[ixj] = a; }
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = 0; r < nrows; ++r) {
+    RowCut rc{};
+    if (ok[r])
+      ok[r] = window_cut(tk_sortb(smem, r), total[r], n_pad[r], st[r]->m, c, st[r]->s_f, smp, sh,
+                         rc);
+    if (ok[r]) set_cut(*st[r], rc);
+  }
+  // p's kept set is among its K largest tokens, all in the CTAs' lists
+  p_listed = ok[0];
+  for (int r = 0; r < nrows; ++r) {
+    if (ok[r]) continue;
+    RowCut rc;
+    if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, smp, rc))
+      return false;
+    set_cut(*st[r], rc);
+  }
+  return true;
+}
+
 // Visited-rows-only schedule: the statistics the dense row pass would have written
 // for the p row (and the q row when with_q) of a node the walk visits, computed by
 // the cluster.  Every CTA covers its slice with a running maximum (its first index)
@@ -1710,9 +2115,15 @@ template <typename T>
 __device__ bool cluster_cut(const TreeJob& job, const void* prow, const void* qrow, bool with_q,
                             spec_row_stats& sp, spec_row_stats& sq, int ua, int ub,
                             unsigned char* smem, uint32_t n_visit, CShared& sh, int C,
-                            uint32_t rank, uint32_t& n_ex, const Samp& smp, bool& p_listed) {
+                            uint32_t rank, uint32_t& n_ex, const Samp& smp, bool& p_listed,
+                            const uint64_t*& p_list) {
   p_listed = false;
+  p_list = nullptr;
   if constexpr (sizeof(T) == 2) {
+    if (!job.exact && smp.top_k > 0 && smp.top_k <= kTopkList)
+      return cluster_cut_topk(job, prow, qrow, with_q, sp, sq, ua, ub, smem, n_visit, sh, C, rank,
+                              n_ex, smp, p_listed, p_list);
+    p_list = bf16_cand_list(smem, 0);
     return cluster_cut_bf16(job, prow, qrow, with_q, sp, sq, ua, ub, smem, sh, C, rank, n_ex, smp,
                             p_listed);
   } else {
@@ -1883,6 +2294,9 @@ constexpr size_t cut_smem_bytes() {
                    2 * (size_t)kCandCTA * sizeof(uint64_t)
              : (4 * (size_t)kCandCTA + 2 * (size_t)kSortW) * sizeof(uint64_t);
 }
+static_assert(kTkSmemBytes <= cut_smem_bytes<uint16_t>(),
+              "the top-k route's buffers fit in the bf16 cut's shared memory");
+static_assert(kTopkList <= kCandCTA / 2, "a compacted list keeps room for a round");
 
 // ---------------------------------------------------------------------------
 // Sampling walk: one cluster of C CTAs per tree.
@@ -2030,10 +2444,11 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       if (r == 0) sh.kid_u[i] = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
     }
     bool p_listed = false;  // kept-set mode for this node
+    const uint64_t* p_list = nullptr;  // this CTA's list of p's window tokens
     if (smp.trunc) {
       // cut the visited rows
       if (!cluster_cut<T>(job, prow, qrow, c1 > c0, sp, sq, ua, ub, cut_smem, n_visit++, sh, C,
-                          rank, n_ex, smp, p_listed)) {
+                          rank, n_ex, smp, p_listed, p_list)) {
         timed_out = true;
         status = SPEC_ROW_TIMEOUT;
         break;
@@ -2049,7 +2464,7 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     // this node streams no row again)
     const KeptSet ks = KeptSet::in_ring(ring);
     if (p_listed)
-      build_kept<T>(job, bf16_cand_list(cut_smem, 0), min(sh.ncand[0], (unsigned)kCandCTA), qrow,
+      build_kept<T>(job, p_list, min(sh.ncand[0], (unsigned)kCandCTA), qrow,
                     c1 > c0, sp, sq, fp, fq, ks, sh);
     int j = 0, next = -1;
     for (int i = c0; i < c1; ++i) {

@@ -223,6 +223,86 @@ def test_benchmarked_workload_every_tree(name, seed, min_compared):
     assert len(sel) == w.B and n >= min_compared, (n, ex)
 
 
+# --- the top-k route of bf16 rows (per-CTA lists under a rising threshold) ----------
+
+@pytest.mark.parametrize("w", [
+    W["tree26_b256_v152064"].with_(B=32, top_k=128),
+    W["tree26_b256_v152064"].with_(B=32, top_k=129),
+    W["tree26_b256_v152064"].with_(B=300, N=6, V=3001, depth=3, top_k=5, top_p=1.0),
+    W["tree60_b64_v128256"].with_(B=16, top_k=20),
+    W["tree60_b64_v128256"].with_(B=16, V=9000, top_k=1, top_p=0.5),
+], ids=["k128-largest-listed", "k129-window-route", "k5-ragged-one-cta", "gauss-k20-topp",
+        "k1"])
+def test_topk_route(w):
+    _parity(w, seed=41)
+
+
+def test_topk_route_equals_exact_selection():
+    w = W["tree26_b256_v152064"].with_(B=16, V=40000)
+    inp = gpu_inputs(w, 12)
+    a = run_gpu(w, inp, seed=13)
+    b = run_gpu(w, inp, seed=13, flags=binding.SPEC_FLAG_EXACT_SELECT)
+    for key in ("accept_len", "tokens", "path", "status"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_array_equal(a["alpha"], b["alpha"])
+    # every cut row took the list route; the flag sent every one to the exact selection
+    assert a["counters"]["fallback_rows"] == 0 and b["counters"]["fallback_rows"] > 0
+
+
+@pytest.mark.parametrize("levels,k", [(6, 100), (200, 50), (2, 3), (0, 100)])
+def test_topk_route_ties(levels, k):
+    """Logits on a coarse grid tie in large groups at the k-th key: the cut is the
+    k-th token in (logit desc, index asc) order whether the lists hold the tied group
+    or leave the row to the exact selection (levels 0: every p logit ties, more than
+    a list holds)."""
+    rng = np.random.default_rng(levels)
+    B, N, V = 12, 7, 20000
+    par = np.stack([wl.random_tree(N, 3, 3, rng) for _ in range(B)])
+
+    def grid(x):
+        return np.zeros_like(x) if levels == 0 else np.round(x * levels / 6) * 6 / levels
+
+    p = grid(rng.normal(0, 2, size=(B, N, V))).astype(np.float32)
+    q = np.round(rng.normal(0, 2, size=(B, N, V)) * 2).astype(np.float32) / 2
+    ph = torch.as_tensor(p).to(torch.bfloat16)
+    qh = torch.as_tensor(q).to(torch.bfloat16)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    out = binding.verify_tree(_dev_rows(ph), _dev_rows(qh), torch.as_tensor(tok, device=DEV),
+                              torch.as_tensor(par, device=DEV), 3, 1.0, k, 0.905, seed=3)
+    torch.cuda.synchronize()
+    gpu = {a: b.cpu().numpy() for a, b in out.items()}
+    ref = oracle.verify_tree(wl.host_logits(ph), wl.host_logits(qh), tok, par, 3, 1.0, k, 0.905,
+                             seed=3)
+    _assert_same(gpu, ref)
+    assert (ref["near"] == 0).sum() >= B // 2
+
+
+def test_topk_route_far_kth_token():
+    """An outlier maximum puts the k-th largest logit far below the window's floor
+    (m - 9 T): the lists are collected again with no floor and the rows still
+    take the list route."""
+    rng = np.random.default_rng(17)
+    B, N, V, k = 10, 6, 30000, 40
+    par = np.stack([wl.random_tree(N, 3, 2, rng) for _ in range(B)])
+    p = rng.normal(0, 1, size=(B, N, V)).astype(np.float32)
+    q = rng.normal(0, 1, size=(B, N, V)).astype(np.float32)
+    p[:, :, 7] = 25.0
+    q[:, :, 11] = 20.0
+    ph = torch.as_tensor(p).to(torch.bfloat16)
+    qh = torch.as_tensor(q).to(torch.bfloat16)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    tok[:, 1::2] = 7
+    out = binding.verify_tree(_dev_rows(ph), _dev_rows(qh), torch.as_tensor(tok, device=DEV),
+                              torch.as_tensor(par, device=DEV), 3, 1.0, k, 1.0, seed=5,
+                              want_counters=True)
+    torch.cuda.synchronize()
+    gpu = {a: (b.cpu().numpy() if torch.is_tensor(b) else b) for a, b in out.items()}
+    ref = oracle.verify_tree(wl.host_logits(ph), wl.host_logits(qh), tok, par, 3, 1.0, k, 1.0,
+                             seed=5)
+    _assert_same(gpu, ref)
+    assert gpu["counters"]["fallback_rows"] == 0
+
+
 def test_exact_select_flag_gives_identical_outputs():
     w = W["tree60_b64_v128256"].with_(B=6, V=40000)
     inp = gpu_inputs(w, 5)

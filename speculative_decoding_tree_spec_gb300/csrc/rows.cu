@@ -143,6 +143,22 @@ template <int MODE>
 __host__ __device__ constexpr size_t ring_bytes() { return (size_t)ring_stages<MODE>() * kStageBytes; }
 template <int MODE>
 __host__ __device__ constexpr size_t bar_bytes() { return (size_t)ring_stages<MODE>() * 16; }
+
+// Balanced schedule of a tree launch's rows (sampling without a cut, the verify
+// step's dense pass): the draft row of a node without children is never read, so
+// every G-th virtual row would give the blocks unequal numbers of real rows.  Each
+// block instead lists the rows it streams: every G-th of the needed rows, in virtual
+// order, from its own index.  Its buffers (small: four blocks per SM must still fit):
+// the needed-draft-row bit mask, the words' exclusive population prefix (+ the
+// total), and the block's list of rows.
+constexpr int kSchedMaxNodes = 16384;  // B * N the schedule covers
+constexpr int kSchedWords = kSchedMaxNodes / 32;
+constexpr int kSchedRows = 64;         // rows of one block
+constexpr int kSchedBatch = 8;         // parent entries one thread loads at once
+template <int MODE>
+__host__ __device__ constexpr size_t sched_bytes() {
+  return MODE == 1 ? (size_t)kSchedWords * 4 + (size_t)(kSchedWords + 2) * 2 + kSchedRows * 4 : 0;
+}
 constexpr size_t kScratchBytes = (size_t)kHistBins * 12 + (size_t)kTieCap * 4 > (size_t)kSortCap * 8
                                      ? (size_t)kHistBins * 12 + (size_t)kTieCap * 4
                                      : (size_t)kSortCap * 8;
@@ -152,7 +168,8 @@ __host__ __device__ constexpr size_t cand_bytes() {
 }
 template <typename T, int MODE>
 __host__ __device__ constexpr size_t row_dyn_smem() {
-  return ring_bytes<MODE>() + bar_bytes<MODE>() + (MODE == 2 ? cand_bytes<T>() + kScratchBytes : 0);
+  return ring_bytes<MODE>() + bar_bytes<MODE>() + (MODE == 2 ? cand_bytes<T>() + kScratchBytes : 0) +
+         sched_bytes<MODE>();
 }
 
 // 16-bit order key of the bf16 logit with raw bits b.
@@ -238,6 +255,89 @@ __device__ __forceinline__ uint32_t window_slot(int bit, int& k, int& e) {
   }
 }
 
+__device__ __forceinline__ bool use_schedule(const RowJob& job, int MODE, int G) {
+  if (MODE != 1 || job.mode != kRowsTree || !job.with_q) return false;
+  const int BN = job.B * job.N;
+  return BN <= kSchedMaxNodes && (2 * BN + G - 1) / G <= kSchedRows;
+}
+
+// Every thread of the block: the rows this block streams, in order, into rows[];
+// returns their number.  A draft row is needed when its node has a child (a later
+// node naming it as parent) and the tree is sampled.
+__device__ int build_schedule(const RowJob& job, uint32_t* mask, uint16_t* pre, int* rows) {
+  const int lane = threadIdx.x & 31;
+  const int BN = job.B * job.N;
+  const int nwords = (BN + 31) >> 5;
+  const int p_lo = min(job.first_row, BN);   // first target row of the launch
+  const int P = BN - p_lo;                    // its target rows
+  const int q_lo = max(job.first_row - BN, 0);  // first draft row (as a node index)
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) mask[w] = 0u;
+  __syncthreads();
+  // the parent entries are loaded kSchedBatch at a time (independent loads in flight)
+  for (int i0 = 0; i0 < BN; i0 += kSchedBatch * (int)blockDim.x) {
+    int par[kSchedBatch];
+    float temp[kSchedBatch];
+#pragma unroll
+    for (int k = 0; k < kSchedBatch; ++k) {
+      const int i = i0 + k * (int)blockDim.x + (int)threadIdx.x;
+      par[k] = i < BN ? job.parents[i] : -1;
+      temp[k] = (i < BN && job.req_temperature) ? job.req_temperature[i / job.N] : 1.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kSchedBatch; ++k) {
+      const int i = i0 + k * (int)blockDim.x + (int)threadIdx.x;
+      if (i >= BN) continue;
+      const int b = i / job.N, ch = i - b * job.N;
+      // a child (a node after its parent) of a sampled tree
+      if (ch == 0 || par[k] < 0 || par[k] >= ch || !(temp[k] > 0.0f)) continue;
+      const int r = b * job.N + par[k];
+      if (r >= q_lo) atomicOr(&mask[r >> 5], 1u << (r & 31));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t run = 0;
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const int w = w0 + lane;
+      const uint32_t c = w < nwords ? (uint32_t)__popc(mask[w]) : 0u;
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (w < nwords) pre[w] = (uint16_t)(run + incl - c);
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) pre[nwords] = (uint16_t)run;
+  }
+  __syncthreads();
+  const int total = P + (int)pre[nwords];
+  const int G = (int)gridDim.x;
+  const int n_mine = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / G + 1 : 0;
+  for (int i = threadIdx.x; i < n_mine; i += blockDim.x) {
+    const int j = (int)blockIdx.x + i * G;
+    int v;
+    if (j < P) {
+      v = p_lo + j;
+    } else {
+      // the word holding the t-th needed draft row: the last word whose prefix is <= t
+      const uint32_t t = (uint32_t)(j - P);
+      int lo = 0, hi = nwords - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      uint32_t m = mask[lo];
+      for (uint32_t k = t - pre[lo]; k > 0 && m; --k) m &= m - 1u;  // drop the lower bits
+      v = BN + lo * 32 + (m ? __ffs(m) - 1 : 0);
+    }
+    rows[i] = v;
+  }
+  __syncthreads();
+  return n_mine;
+}
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_kernel(RowJob job) {
   constexpr int E = Elt<T>::kPerUnit;
@@ -288,12 +388,29 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
     fence_barrier_init();
   }
   __syncthreads();
+  // the balanced schedule (modes 0 and 2 and list launches: every G-th virtual row)
+  const bool sched = use_schedule(job, MODE, (int)gridDim.x);
+  int* const sched_rows = reinterpret_cast<int*>(
+      dyn + row_dyn_smem<T, MODE>() - (size_t)kSchedRows * 4);
+  int n_mine = 0;
+  if (sched) {
+    uint32_t* const mask = reinterpret_cast<uint32_t*>(dyn + row_dyn_smem<T, MODE>() -
+                                                       sched_bytes<MODE>());
+    n_mine = build_schedule(job, mask, reinterpret_cast<uint16_t*>(mask + kSchedWords), sched_rows);
+  }
 
   if (warp == NW) {
     // ---------------- producer warp ----------------
     uint32_t g = 0;  // chunks issued so far (the same count the consumers walk)
     bool stop = false;
-    for (int v = job.first_row + (int)blockIdx.x; v < total && !stop; v += gridDim.x) {
+    for (int i = 0, v0 = job.first_row + (int)blockIdx.x; !stop; ++i, v0 += gridDim.x) {
+      int v = v0;
+      if (sched) {
+        if (i >= n_mine) break;
+        v = sched_rows[i];
+      } else if (v0 >= total) {
+        break;
+      }
       const char* row;
       if (job.mode == kRowsList) {
         row = static_cast<const char*>(row_ptr(job.base_p, (int64_t)v * job.row_pitch, Elt<T>::kBytes));
@@ -301,8 +418,8 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
         const bool is_q = v >= BN;
         const int r = is_q ? v - BN : v;
         const int b = r / job.N, n = r - b * job.N;
-        if (is_q && job.req_temperature && !(job.req_temperature[b] > 0.0f)) continue;
-        if (is_q) {
+        if (!sched && is_q && job.req_temperature && !(job.req_temperature[b] > 0.0f)) continue;
+        if (is_q && !sched) {
           int has_child = 0;
           for (int ch = n + 1 + lane; ch < job.N; ch += 32)
             has_child |= (job.parents[(int64_t)b * job.N + ch] == n);
@@ -353,7 +470,14 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
 
   // ---------------- consumer threads ----------------
   uint32_t g = 0;
-  for (int v = job.first_row + (int)blockIdx.x; v < total; v += gridDim.x) {
+  for (int i = 0, v0 = job.first_row + (int)blockIdx.x;; ++i, v0 += gridDim.x) {
+    int v = v0;
+    if (sched) {
+      if (i >= n_mine) break;
+      v = sched_rows[i];
+    } else if (v0 >= total) {
+      break;
+    }
     const void* row;
     spec_row_stats* out;
     float c = c_launch;
@@ -372,7 +496,7 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
         if (is_q && !(temp > 0.0f)) continue;
         c = sampled ? (float)(1.4426950408889634 / (double)temp) : 1.0f;
       }
-      if (is_q) {
+      if (is_q && !sched) {
         // the draft row of node n is read only if some node has n as its parent
         // (every warp decides for itself, identically)
         int has_child = 0;

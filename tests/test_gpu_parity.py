@@ -223,6 +223,60 @@ def test_benchmarked_workload_every_tree(name, seed, min_compared):
     assert len(sel) == w.B and n >= min_compared, (n, ex)
 
 
+# --- the dense pass of a tree launch reads exactly the rows the walk may need -------
+
+@pytest.mark.parametrize("per_request", [False, True])
+def test_tree_row_pass_reads_exactly_the_needed_rows(per_request):
+    """Every target row's statistics, and those of the draft rows of nodes with a
+    child (of sampled trees), equal spec_filter_rows' on the same rows; no other draft
+    row is written.  (The statistics sit at the start of the workspace: B*N target
+    records, then, 256-byte aligned, B*N draft records.)"""
+    w = W["tree60_b64_v128256"].with_(V=32000)
+    B, N, V = w.B, w.N, w.V
+    inp = gpu_inputs(w, 3)
+    ws = torch.full((binding.workspace_size(B, N, V),), 0xAB, dtype=torch.uint8, device=DEV)
+    phases = binding.SPEC_PHASE_PREPARE | binding.SPEC_PHASE_ROWS
+    temps = np.array([0.0 if (per_request and b % 3 == 0) else 0.7 for b in range(B)],
+                     np.float32)
+    if per_request:
+        binding.verify_tree_per_request(inp["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
+                                        inp["max_depth"], torch.as_tensor(temps, device=DEV),
+                                        workspace=ws, phases=phases)
+    else:
+        binding.verify_tree(inp["p"], inp["q"], inp["tokens_d"], inp["parents_d"],
+                            inp["max_depth"], 0.7, workspace=ws, phases=phases)
+    torch.cuda.synchronize()
+    BN = B * N
+    off_q = (BN * 32 + 255) // 256 * 256
+    got_p = ws[:BN * 32].view(BN, 32).cpu().numpy()
+    got_q = ws[off_q:off_q + BN * 32].view(BN, 32).cpu().numpy()
+    rows = {k: inp[k].as_strided((BN, V), (inp[k].stride(1), 1)) for k in ("p", "q")}
+    ref = {}
+    for k in ("p", "q"):
+        st = torch.empty((BN, 32), dtype=torch.uint8, device=DEV)
+        assert binding.lib().spec_filter_rows(rows[k].data_ptr(), binding._dtype_code(rows[k]),
+                                              BN, V, rows[k].stride(0),
+                                              binding.params(0.7, 0, 1.0, 0), st.data_ptr(),
+                                              0) == 0
+        torch.cuda.synchronize()
+        ref[k] = st.cpu().numpy()
+    par = inp["parents"]
+    has_child = np.zeros((B, N), bool)
+    for b in range(B):
+        for ch in range(1, N):
+            if 0 <= par[b, ch] < ch:
+                has_child[b, par[b, ch]] = True
+    sampled = np.repeat(temps > 0, N)
+    need_q = has_child.reshape(-1) & sampled
+    # target rows: every record (greedy trees: the maximum and its index)
+    np.testing.assert_array_equal(got_p[sampled], ref["p"][sampled])
+    g = got_p[~sampled].view(np.int32)
+    r = ref["p"][~sampled].view(np.int32)
+    np.testing.assert_array_equal(g[:, [0, 6]], r[:, [0, 6]])
+    np.testing.assert_array_equal(got_q[need_q], ref["q"][need_q])
+    assert (got_q[~need_q] == 0xAB).all()
+
+
 # --- the top-k route of bf16 rows (per-CTA lists under a rising threshold) ----------
 
 @pytest.mark.parametrize("w", [

@@ -463,6 +463,32 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 
 // Slots for n items per lane from a shared counter, one atomic per warp (every lane
 // of the warp calls it): the first of this lane's slots.
+// Shared-memory add with no result (a reduction on a shared-window address).
+__device__ __forceinline__ void red_add_shared(unsigned* p, unsigned v) {
+  asm volatile("red.shared.add.u32 [%0], %1;\n" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// Bits e (0..7) of a unit's bf16 logits that are >= t, t a bf16 pair of one value:
+// two logits per compare (for bf16 z and fp32 thr, z >= thr iff z >= thr rounded up
+// to bf16; -0 and +0 compare equal, as their order keys do).
+__device__ __forceinline__ uint32_t unit_ge_bits(const uint4& v, __nv_bfloat162 t) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t mk = __hge2_mask(as_bf2(w[q]), t);
+    m |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * q);
+  }
+  return m;
+}
+// Order key of element e (a runtime index, 0..7) of a unit of bf16 logits, selected
+// from the packed words (no array indexed at run time).
+__device__ __forceinline__ uint32_t unit_key(const uint4& v, int e) {
+  const uint32_t w = (e & 4) ? ((e & 2) ? v.w : v.z) : ((e & 2) ? v.y : v.x);
+  const uint32_t b = (e & 1) ? (w >> 16) : (w & 0xffffu);
+  return order_key(__uint_as_float(b << 16));
+}
+
 __device__ __forceinline__ unsigned warp_reserve(unsigned* ctr, unsigned n) {
   const int lane = threadIdx.x & 31;
   unsigned incl = n;
@@ -516,6 +542,9 @@ struct CShared {
   unsigned kp_n;    // this CTA's kept tokens of p (kept-set mode)
   unsigned long long ured[CW];
   int kp_tok;
+  // window-pass staging: the two stages' barriers, rounds staged so far
+  uint64_t wbar[2];
+  uint32_t win_g;
   // top-k route: per row, the list threshold (an order key) and the selection digits
   uint32_t tk_thr[2];
   int tk_d1[2];
@@ -885,20 +914,91 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
       unsigned base = 0u;
       if (lane == 0) base = atomicAdd(&sh.ncand[r], total);
       base = __shfl_sync(kFull, base, 0) + incl - mine;
-      while (bits) {
-        const int e = __ffs(bits) - 1;
-        bits &= bits - 1;
+      // elements by compile-time index (a runtime index would put z in local memory)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (!((bits >> e) & 1u)) continue;
         const uint32_t k = order_key(z[e]);
         if (base < (unsigned)kCandCTA)
           cand[r][base] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * E + e));
         ++base;
         if (hist[r]) {
           const uint32_t bin = k16m[r] - (k >> 16);
-          if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
+          if (bin < (uint32_t)kWalkBins) red_add_shared(&hist[r][bin], 1u);
         }
       }
     }
   });
+}
+
+constexpr int kWinUnits = 4;  // units of each row per thread and round of a window pass
+
+// Window-pass staging.  A bf16 window pass reads its slice of one or two rows in
+// rounds of CT * kWinUnits whole units per row.  With a 64 KB streaming ring the
+// rounds arrive by bulk copy in two 32 KB stages, thread 0 issuing each round two
+// rounds ahead: one round is filtered while the next two are in flight (twice the
+// bytes in flight of loads into registers).  Rounds are counted over the kernel
+// (sh.win_g): round g uses stage g & 1 and completes that stage's barrier phase
+// (g >> 1) & 1.
+struct WinStage {
+  const uint4* src[2];
+  int nrows, ua, ubf, nfull;  // nfull: rounds of whole units
+  uint32_t g0;
+  bool on;
+  __device__ uint4* slot(CShared& sh, int rd, int r) const {
+    return sh.ring + ((size_t)((g0 + (uint32_t)rd) & 1u) * 2 + (size_t)r) * (CT * kWinUnits);
+  }
+  // thread 0: the bulk copies of round rd
+  __device__ void issue(CShared& sh, int rd) const {
+    const uint32_t st = (g0 + (uint32_t)rd) & 1u;
+    const int base = ua + rd * CT * kWinUnits;
+    const uint32_t bytes = (uint32_t)min(CT * kWinUnits, ubf - base) * 16u;
+    mbar_arrive_expect_tx(&sh.wbar[st], bytes * (uint32_t)nrows);
+    for (int r = 0; r < nrows; ++r) bulk_copy_g2s(slot(sh, rd, r), src[r] + base, bytes, &sh.wbar[st]);
+  }
+  __device__ bool wait(CShared& sh, int rd) const {
+    const uint32_t g = g0 + (uint32_t)rd;
+    return mbar_wait(&sh.wbar[g & 1u], (g >> 1) & 1u, kExchangeLimitNs);
+  }
+};
+
+// Every thread: the staging of a pass over whole units [ua, ubf) of `nrows` rows;
+// issues its first two rounds.
+__device__ WinStage win_stage_begin(const void* const (&rows)[2], int nrows, int ua, int ubf,
+                                    CShared& sh) {
+  WinStage w;
+  w.src[0] = reinterpret_cast<const uint4*>(rows[0]);
+  w.src[1] = reinterpret_cast<const uint4*>(nrows > 1 ? rows[1] : rows[0]);
+  w.nrows = nrows;
+  w.ua = ua;
+  w.ubf = ubf;
+  w.nfull = ubf > ua ? (ubf - ua + CT * kWinUnits - 1) / (CT * kWinUnits) : 0;
+  w.on = sh.ring_stages == 4 && w.nfull > 0;
+  w.g0 = sh.win_g;
+  if (w.on) {
+    // the ring's earlier contents were written and read through the generic proxy
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      w.issue(sh, 0);
+      if (w.nfull > 1) w.issue(sh, 1);
+    }
+  }
+  return w;
+}
+
+// Every thread, after the pass (or when a stage's wait gave up at round `stop`):
+// the rounds staged so far are recorded; after a failed wait thread 0 first waits,
+// bounded, for the copies still in flight.
+__device__ void win_stage_end(const WinStage& w, CShared& sh, int stop) {
+  if (!w.on) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (stop < w.nfull)
+      for (int rd = stop; rd < min(w.nfull, stop + 2); ++rd) w.wait(sh, rd);
+    sh.win_g = w.g0 + (uint32_t)w.nfull;
+  }
+  __syncthreads();
 }
 
 // bf16 rows, the window pass: units [ua, ub) of one or two rows are read with
@@ -907,9 +1007,8 @@ __device__ void window_collect(const void* const (&rows)[2], int nrows, int V, i
 // bf16 maximum reaches the window threshold.  Tokens z >= thr[r] go to cand[r] (slots
 // reserved once per warp and round; sh.ncand[r] counts all of them, cand[r] keeps
 // the first kCandCTA) and are counted per key in hist[r] (when not null).
-constexpr int kWinUnits = 4;
 
-__device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int V, int ua,
+__device__ bool window_collect_fast(const void* const (&rows)[2], int nrows, int V, int ua,
                                     int ub, const float (&thr)[2], uint64_t* const (&cand)[2],
                                     unsigned* const (&hist)[2], const uint32_t (&k16m)[2],
                                     CShared& sh) {
@@ -917,8 +1016,10 @@ __device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int
   const int ubf = min(ub, full);
   const uint4* const r0 = reinterpret_cast<const uint4*>(rows[0]);
   const uint4* const r1 = reinterpret_cast<const uint4*>(nrows > 1 ? rows[1] : rows[0]);
-  const __nv_bfloat162 t2[2] = {__bfloat162bfloat162(__float2bfloat16_rd(thr[0])),
-                                __bfloat162bfloat162(__float2bfloat16_rd(thr[1]))};
+  const WinStage stg = win_stage_begin(rows, nrows, ua, ubf, sh);
+  int stop = INT_MAX;
+  const __nv_bfloat162 t2[2] = {__bfloat162bfloat162(__float2bfloat16_ru(thr[0])),
+                                __bfloat162bfloat162(__float2bfloat16_ru(thr[1]))};
   // the rounds cover the whole units; the partial last unit (if this slice has it) is
   // one more round of its own, read with element loads
   const int nround = (ubf > ua ? (ubf - ua + CT * kWinUnits - 1) / (CT * kWinUnits) : 0) +
@@ -927,7 +1028,28 @@ __device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int
     const bool tail = ub > full && rd == nround - 1;
     const int base = tail ? full : ua + rd * CT * kWinUnits;
     uint4 raw[2][kWinUnits];
-    if (!tail) {
+    if (!tail && stg.on) {
+      // this round's stage (bounded wait; every thread gives up together)
+      if (!__syncthreads_and(stg.wait(sh, rd))) { stop = rd; break; }
+      const uint4* s0 = stg.slot(sh, rd, 0);
+      const uint4* s1 = stg.slot(sh, rd, 1);
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const int u = base + h * CT + (int)threadIdx.x;
+        const bool in = u < ubf;
+        raw[0][h] = in ? s0[h * CT + threadIdx.x]
+                       : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        raw[1][h] = (in && nrows > 1)
+                        ? s1[h * CT + threadIdx.x]
+                        : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      }
+      // every thread has read the stage: it takes round rd + 2
+      __syncthreads();
+      if (threadIdx.x == 0 && rd + 2 < stg.nfull) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        stg.issue(sh, rd + 2);
+      }
+    } else if (!tail) {
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
         const int u = base + h * CT + (int)threadIdx.x;
@@ -953,16 +1075,7 @@ __device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int
     for (int r = 0; r < 2; ++r)
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
-        const uint4 v = raw[r][h];
-        uint32_t m = 0;
-        const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)),
-                                         __hmax2(as_bf2(v.z), as_bf2(v.w)));
-        if (__hge2_mask(a, t2[r])) {
-          float z[8];
-          Elt<uint16_t>::unpack(v, z);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m |= (z[e] >= thr[r]) ? (1u << e) : 0u;
-        }
+        const uint32_t m = unit_ge_bits(raw[r][h], t2[r]);
         mb[r][h] = m;
         cnt[r] += __popc(m);
       }
@@ -973,14 +1086,11 @@ __device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
         uint32_t bits = mb[r][h];
-        if (!bits) continue;
-        float z[8];
-        Elt<uint16_t>::unpack(raw[r][h], z);
         const int u = tail ? full : base + h * CT + (int)threadIdx.x;
         while (bits) {
           const int e = __ffs(bits) - 1;
           bits &= bits - 1u;
-          const uint32_t k = order_key(z[e]);
+          const uint32_t k = unit_key(raw[r][h], e);
           if (pos < (unsigned)kCandCTA)
             cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
           ++pos;
@@ -992,6 +1102,8 @@ __device__ void window_collect_fast(const void* const (&rows)[2], int nrows, int
       }
     }
   }
+  win_stage_end(stg, sh, stop);
+  return stop == INT_MAX;
 }
 
 // Step 2 after the sort: the cut from n sorted candidates (descending, padded to
@@ -1188,7 +1300,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
   if (!sl) return false;
   unsigned cnt[2][kMaxC], total[2] = {0u, 0u}, n_pad[2] = {2u, 2u};
   bool fast[2] = {false, false};
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     bool over = false;
     for (int q = 0; q < C; ++q) {
       cnt[r][q] = (unsigned)(sl[q][0] >> (32 * r));
@@ -1201,7 +1315,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
     while (n_pad[r] < total[r]) n_pad[r] <<= 1;
   }
   // gather every CTA's candidates (remote shared memory) into the sort buffers
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     if (!fast[r]) continue;
     uint64_t* keys = sortb + r * kSortW;
     for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
@@ -1218,7 +1334,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
   const unsigned pad_max = max(fast[0] ? n_pad[0] : 0u, fast[1] ? n_pad[1] : 0u);
   for (unsigned k = 2; k <= pad_max; k <<= 1) {  // bitonic sort, descending
     for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (!fast[r] || k > n_pad[r]) continue;
         uint64_t* keys = sortb + r * kSortW;
         for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
@@ -1233,7 +1351,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
       __syncthreads();
     }
   }
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     spec_row_stats& s = *st[r];
     RowCut rc{};
     bool ok = fast[r] && window_cut(sortb + r * kSortW, total[r], n_pad[r], s.m, c, s.s_f, smp,
@@ -1409,7 +1529,8 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   }
   if (threadIdx.x == 0) { sh.ncand[0] = 0u; sh.ncand[1] = 0u; }
   __syncthreads();
-  if (!job.exact) window_collect_fast(rows, nrows, V, ua, ub, thr, cl, hp, k16m, sh);
+  if (!job.exact && !window_collect_fast(rows, nrows, V, ua, ub, thr, cl, hp, k16m, sh))
+    return false;
   __syncthreads();
   const unsigned own_n[2] = {min(sh.ncand[0], (unsigned)kCandCTA), min(sh.ncand[1], (unsigned)kCandCTA)};
   // a CTA whose list overflowed finds the cut key's members by a pass over its slice
@@ -1421,9 +1542,13 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   bool p_all_listed = !job.exact;
   for (int q = 0; q < C; ++q) p_all_listed &= (unsigned)sl[q][0] <= (unsigned)kCandCTA;
   bool win[2] = {false, false};
-  for (int r = 0; r < nrows; ++r) win[r] = !job.exact && fits[r];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+    if (r < nrows) win[r] = !job.exact && fits[r];
   // merge the key counts of every CTA (same order, integer sums: identical everywhere)
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     if (!win[r]) continue;
     for (int i = threadIdx.x; i < nb[r]; i += CT) {
       // every peer's count is requested before any is added (the loads overlap)
@@ -1448,11 +1573,15 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   if (threadIdx.x < 2) { sh.tie_cnt[threadIdx.x] = 0u; sh.tie_max[threadIdx.x] = -1; }
   __syncthreads();
   bool ok[2] = {false, false};
-  for (int r = 0; r < nrows; ++r) ok[r] = sh.sc_ok[r] != 0;
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+    if (r < nrows) ok[r] = sh.sc_ok[r] != 0;
   uint32_t cut32[2] = {0u, 0u};
   if (ok[0] || ok[1]) {
     // members of the cut key in this CTA's candidate list
-    for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
       if (!ok[r]) continue;
       cut32[r] = key_from16(k16m[r] - (uint32_t)sh.sc_bin[r]);
       if (own_over[r]) {
@@ -1488,7 +1617,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
     unsigned jr[2] = {0u, 0u};
     int cut_idx[2] = {0, 0};
     bool need = false;
-    for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
       if (!ok[r]) continue;
       if (sh.sc_j[r] == sh.sc_ncut[r]) {
         int mx = -1;
@@ -1509,7 +1640,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
       // merged counts are no longer needed and hold the owner's member indices
       if (threadIdx.x < 2) { sh.mem_n[threadIdx.x] = 0u; sh.tie_idx[threadIdx.x] = -1; }
       __syncthreads();
-      for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (owner[r] != (int)rank) continue;
         // gather this CTA's members of the cut key (at most kWalkBins of them;
         // more leaves the row to the exact selection)
@@ -1535,7 +1668,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
         }
       }
       __syncthreads();
-      for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (owner[r] != (int)rank) continue;
         const unsigned nm = sh.mem_n[r];
         if (nm > (unsigned)kWalkBins) continue;  // tie_idx stays -1: the exact selection decides
@@ -1552,13 +1687,17 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
         if (owner[r] == (int)rank) iw[r] = (uint64_t)(uint32_t)sh.tie_idx[r];
       const SlotRow* xs = cluster_share(iw, 2, sh, C, rank, n_ex);
       if (!xs) return false;
-      for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (!ok[r] || owner[r] < 0) continue;
         cut_idx[r] = (int)(uint32_t)xs[owner[r]][r];
         if (cut_idx[r] < 0) ok[r] = false;  // too many tied members: exact selection
       }
     }
-    for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
       if (!ok[r]) continue;
       RowCut rc;
       rc.key = cut32[r];
@@ -1570,7 +1709,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
   }
   // p's kept set lies in the window (its cut came from it) and in the CTAs' lists
   p_listed = ok[0] && p_all_listed;
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     if (ok[r]) continue;
     RowCut rc;
     if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, smp, rc))
@@ -1701,20 +1842,43 @@ __device__ __noinline__ void tk_compact(uint64_t* list, unsigned n, unsigned K, 
 // A round whose tokens overflow a list raises the threshold and re-inserts them
 // from registers; a list past half full is compacted between rounds.  fail[r] is
 // set when kTkRetry raises do not make room (ties at one key).
-__device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int ua, int ub,
+__device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int ua, int ub,
                            uint64_t* const (&list)[2], unsigned K, unsigned* const (&hist)[2],
                            CShared& sh, bool (&fail)[2]) {
   const int full = V / 8;
   const int ubf = min(ub, full);
   const uint4* const r0 = reinterpret_cast<const uint4*>(rows[0]);
   const uint4* const r1 = reinterpret_cast<const uint4*>(nrows > 1 ? rows[1] : rows[0]);
+  const WinStage stg = win_stage_begin(rows, nrows, ua, ubf, sh);
+  int stop = INT_MAX;
   const int nround = (ubf > ua ? (ubf - ua + CT * kWinUnits - 1) / (CT * kWinUnits) : 0) +
                      (ub > full ? 1 : 0);
   for (int rd = 0; rd < nround; ++rd) {  // the same rounds in every thread
     const bool tail = ub > full && rd == nround - 1;
     const int base = tail ? full : ua + rd * CT * kWinUnits;
     uint4 raw[2][kWinUnits];
-    if (!tail) {
+    if (!tail && stg.on) {
+      // this round's stage (bounded wait; every thread gives up together)
+      if (!__syncthreads_and(stg.wait(sh, rd))) { stop = rd; break; }
+      const uint4* s0 = stg.slot(sh, rd, 0);
+      const uint4* s1 = stg.slot(sh, rd, 1);
+#pragma unroll
+      for (int h = 0; h < kWinUnits; ++h) {
+        const int u = base + h * CT + (int)threadIdx.x;
+        const bool in = u < ubf;
+        raw[0][h] = in ? s0[h * CT + threadIdx.x]
+                       : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+        raw[1][h] = (in && nrows > 1)
+                        ? s1[h * CT + threadIdx.x]
+                        : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
+      }
+      // every thread has read the stage: it takes round rd + 2
+      __syncthreads();
+      if (threadIdx.x == 0 && rd + 2 < stg.nfull) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        stg.issue(sh, rd + 2);
+      }
+    } else if (!tail) {
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
         const int u = base + h * CT + (int)threadIdx.x;
@@ -1739,22 +1903,15 @@ __device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int u
     uint32_t drop[2][kWinUnits];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
+      // the threshold key's value rounded up to bf16: a bf16 logit reaches the key
+      // exactly when it reaches that value
       const uint32_t thr = sh.tk_thr[r];
-      const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rd(key_value(thr)));
+      const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_ru(key_value(thr)));
       uint32_t mb[kWinUnits];
       unsigned cnt = 0;
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
-        const uint4 v = raw[r][h];
-        uint32_t m = 0;
-        const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)),
-                                         __hmax2(as_bf2(v.z), as_bf2(v.w)));
-        if (r < nrows && !fail[r] && __hge2_mask(a, t2)) {
-          float z[8];
-          Elt<uint16_t>::unpack(v, z);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m |= (order_key(z[e]) >= thr) ? (1u << e) : 0u;
-        }
+        const uint32_t m = (r < nrows && !fail[r]) ? unit_ge_bits(raw[r][h], t2) : 0u;
         mb[h] = m;
         drop[r][h] = 0u;
         cnt += __popc(m);
@@ -1764,15 +1921,12 @@ __device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int u
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) {
         uint32_t bits = mb[h];
-        if (!bits) continue;
-        float z[8];
-        Elt<uint16_t>::unpack(raw[r][h], z);
         const int u = tail ? full : base + h * CT + (int)threadIdx.x;
         while (bits) {
           const int e = __ffs(bits) - 1;
           bits &= bits - 1u;
           if (pos < (unsigned)kCandCTA)
-            list[r][pos] = ((uint64_t)order_key(z[e]) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+            list[r][pos] = ((uint64_t)unit_key(raw[r][h], e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
           else
             drop[r][h] |= 1u << e;
           ++pos;
@@ -1810,11 +1964,12 @@ __device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int u
         for (int h = 0; h < kWinUnits; ++h) {
           uint32_t bits = drop[r][h], keep = 0u;
           if (bits) {
-            float z[8];
-            Elt<uint16_t>::unpack(unit(h), z);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (((bits >> e) & 1u) && order_key(z[e]) >= thr) keep |= 1u << e;
+            const uint4 v = unit(h);
+            while (bits) {
+              const int e = __ffs(bits) - 1;
+              bits &= bits - 1u;
+              if (unit_key(v, e) >= thr) keep |= 1u << e;
+            }
           }
           drop[r][h] = keep;
           cnt += __popc(keep);
@@ -1824,14 +1979,13 @@ __device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int u
         for (int h = 0; h < kWinUnits; ++h) {
           uint32_t bits = drop[r][h], left = 0u;
           if (!bits) continue;
-          float z[8];
-          Elt<uint16_t>::unpack(unit(h), z);
+          const uint4 v = unit(h);
           const int u = tail ? full : base + h * CT + (int)threadIdx.x;
           while (bits) {
             const int e = __ffs(bits) - 1;
             bits &= bits - 1u;
             if (pos < (unsigned)kCandCTA)
-              list[r][pos] = ((uint64_t)order_key(z[e]) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+              list[r][pos] = ((uint64_t)unit_key(v, e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
             else
               left |= 1u << e;
             ++pos;
@@ -1846,6 +2000,8 @@ __device__ void tk_collect(const void* const (&rows)[2], int nrows, int V, int u
       __syncthreads();
     }
   }
+  win_stage_end(stg, sh, stop);
+  return stop == INT_MAX;
 }
 
 // The cut of the p row (and of the q row when with_q) under top-k by the route
@@ -1874,7 +2030,7 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
   }
   __syncthreads();
   bool fail[2] = {false, nrows < 2};
-  tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, fail);
+  if (!tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, fail)) return false;
   // every CTA's list sizes (all ones: the row failed somewhere)
   auto exchange = [&](unsigned (&total)[2], bool (&bad)[2], unsigned (&cnt)[2][kMaxC]) -> bool {
     uint64_t w = 0;
@@ -1909,7 +2065,7 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
     }
     __syncthreads();
     bool again[2] = {!redo[0], !redo[1]};  // rows set here are skipped
-    tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, again);
+    if (!tk_collect(rows, nrows, V, ua, ub, list, K, hist, sh, again)) return false;
     for (int r = 0; r < 2; ++r)
       if (redo[r]) fail[r] = again[r];
     if (!exchange(total, bad, cnt)) return false;
@@ -1919,8 +2075,9 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
   if ((ok[0] && total[0] > (unsigned)kTkSort) || (ok[1] && total[1] > (unsigned)kTkSort)) {
     // too many to sort: each CTA keeps its own K largest (the lists were final at
     // the exchange; they change only now, and are read after the next one)
-    for (int r = 0; r < nrows; ++r)
-      if (ok[r] && sh.ncand[r] > K) tk_compact(list[r], sh.ncand[r], K, hist[r], sh, r);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (r < nrows && ok[r] && sh.ncand[r] > K) tk_compact(list[r], sh.ncand[r], K, hist[r], sh, r);
     if (!exchange(total, bad, cnt)) return false;
     for (int r = 0; r < 2; ++r) ok[r] = ok[r] && !bad[r] && total[r] >= K;
   }
@@ -1930,7 +2087,9 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
     while (n_pad[r] < total[r]) n_pad[r] <<= 1;
   }
   // gather every CTA's list (remote shared memory) into the sort buffers
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     if (!ok[r]) continue;
     uint64_t* keys = tk_sortb(smem, r);
     for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
@@ -1947,7 +2106,9 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
   const unsigned pad_max = max(ok[0] ? n_pad[0] : 0u, ok[1] ? n_pad[1] : 0u);
   for (unsigned k = 2; k <= pad_max; k <<= 1) {  // bitonic sort, descending
     for (unsigned jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (!ok[r] || k > n_pad[r]) continue;
         uint64_t* keys = tk_sortb(smem, r);
         for (unsigned i = threadIdx.x; i < n_pad[r]; i += CT) {
@@ -1962,7 +2123,9 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
       __syncthreads();
     }
   }
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     RowCut rc{};
     if (ok[r])
       ok[r] = window_cut(tk_sortb(smem, r), total[r], n_pad[r], st[r]->m, c, st[r]->s_f, smp, sh,
@@ -1971,7 +2134,9 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
   }
   // p's kept set is among its K largest tokens, all in the CTAs' lists
   p_listed = ok[0];
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     if (ok[r]) continue;
     RowCut rc;
     if (!cluster_exact_cut<uint16_t>(job, rows[r], *st[r], ua, ub, sh, C, rank, n_ex, smp, rc))
@@ -2040,7 +2205,9 @@ __device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const vo
       }
     }
   });
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     const float wm = warp_max(tm[r]);
     FF sv = ks[r].ff();
     if (tm[r] != -CUDART_INF_F && tm[r] != wm) {
@@ -2061,7 +2228,9 @@ __device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const vo
   __syncthreads();
   uint64_t w[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
   if (threadIdx.x == 0) {
-    for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r >= nrows) break;
       float m = -CUDART_INF_F;
       for (int q = 0; q < CW; ++q) m = fmaxf(m, sh.st_m[r][q]);
       double s = 0.0;
@@ -2080,7 +2249,9 @@ __device__ bool cluster_row_stats(const TreeJob& job, const void* prow, const vo
   const SlotRow* sl = cluster_share(w, 4 * nrows, sh, C, rank, n_ex);
   if (!sl) return false;
   spec_row_stats* st[2] = {&sp, &sq};
-  for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows) break;
     float m = -CUDART_INF_F;
     int any_bad = 0;
     for (int q = 0; q < C; ++q) {
@@ -2359,6 +2530,9 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   if (threadIdx.x == 0) {
     mbar_init(&sh.xbar[0], (uint32_t)C);
     mbar_init(&sh.xbar[1], (uint32_t)C);
+    mbar_init(&sh.wbar[0], 1u);
+    mbar_init(&sh.wbar[1], 1u);
+    sh.win_g = 0u;
     sh.err = 0u;
     sh.ring = ring;
     sh.ring_stages = ring_stages;

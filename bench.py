@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--host-threads", type=int, default=0,
                     help="host threads of the oracle legs (reference arm, cpu_baseline); "
                          "0 = every core")
+    ap.add_argument("--ref-seconds", type=float, default=REFERENCE_BUDGET_S,
+                    help="host seconds the reference arm's timed sample may take")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", choices=["verify", "commit", "tree", "draft"], default="verify",
                     help="commit: time the accepted-path commit on a KV cache instead; tree: "
@@ -357,7 +359,7 @@ def run_reference(args):
     per_step = wall_w / n_warm
     # at least two tree-steps per host thread, so that every thread stays busy over the
     # sample; beyond that as many of the requested steps as the time budget allows
-    n_timed = max(2 * threads, min(args.steps, int(REFERENCE_BUDGET_S / max(per_step, 1e-9))))
+    n_timed = max(2 * threads, min(args.steps, int(args.ref_seconds / max(per_step, 1e-9))))
     wall, rows = time_oracle(w, pool, n_timed, threads, args.seed)
     value = rows / wall
     line = {
@@ -370,7 +372,7 @@ def run_reference(args):
                    "step": "one tree verified by the CPU oracle (steps run on a host thread pool)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{n_timed} of the {args.steps} requested tree-steps timed "
-                                   f"(at most {REFERENCE_BUDGET_S:.0f} s of host time), cycling "
+                                   f"(at most {args.ref_seconds:.0f} s of host time), cycling "
                                    f"over {pool['p'].shape[0]} seeded trees of {w.name}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -18,8 +18,15 @@
  *
  * Conventions shared by every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller, unless stated.
- *     The library allocates nothing and keeps no state between calls, apart from
- *     the scratch address that spec_verify_tree_noalloc caches per device.
+ *     The library allocates nothing and carries no result from one call to the
+ *     next.  It does keep small process-wide caches, filled on first use and
+ *     never freed: per device, the SM count, whether each kernel's shared-memory
+ *     limit has been raised (cudaFuncSetAttribute) and the scratch address of
+ *     spec_verify_tree_noalloc; per kernel, its static shared-memory size.  Their
+ *     first fill is not synchronised between host threads (make the first call on
+ *     a device from one thread); afterwards calls from several threads are safe.
+ *     They describe the device and its loaded module: after cudaDeviceReset() in
+ *     this process no entry point may be called again (restart the process).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *     and returns before the GPU work finishes; it never synchronises the device.
  *   - The return value is SPEC_OK (0) or a negative SPEC_ERR_* code.  Argument
@@ -188,7 +195,10 @@ int spec_verify_tree(const void* logits_p, const void* logits_q, spec_dtype dtyp
  *
  * Set-up: the first call on a device, with that device current, looks up the
  * scratch's device address (cudaGetSymbolAddress) and caches it; make that first
- * call before any stream capture begins.  Later calls only launch.
+ * call before any stream capture begins.  Later calls only launch.  The cached
+ * address belongs to the device's current context: after cudaDeviceReset() the
+ * library's module is loaded anew and the address is stale, so no call may follow
+ * a device reset in the same process.
  * Sharing: all calls on one device use the same scratch.  Two calls whose GPU work
  * may overlap (different streams without an ordering event, or concurrent host
  * threads on different streams) race on it and give undefined results; order them

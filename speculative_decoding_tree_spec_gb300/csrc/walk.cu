@@ -1081,23 +1081,29 @@ __device__ bool window_collect_fast(const void* const (&rows)[2], int nrows, int
       }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      if (!__any_sync(kFull, cnt[r] != 0u)) continue;
-      unsigned pos = warp_reserve(&sh.ncand[r], cnt[r]);
+      if (!cnt[r]) continue;
+      // one shared atomic per lane with members (their order in the list is free: every
+      // reader of a list treats it as a set)
+      unsigned pos = atomicAdd(&sh.ncand[r], cnt[r]);
+      // the lane's members over all its units in one loop (bit 8 h + e), so the warp
+      // iterates as often as its busiest lane has members, not once per unit
+      static_assert(kWinUnits * 8 <= 32, "a lane's window bits fit one word");
+      uint32_t bits = 0u;
 #pragma unroll
-      for (int h = 0; h < kWinUnits; ++h) {
-        uint32_t bits = mb[r][h];
+      for (int h = 0; h < kWinUnits; ++h) bits |= mb[r][h] << (8 * h);
+      while (bits) {
+        const int t = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int h = t >> 3, e = t & 7;
+        const uint4 v = h == 0 ? raw[r][0] : h == 1 ? raw[r][1] : h == 2 ? raw[r][2] : raw[r][3];
         const int u = tail ? full : base + h * CT + (int)threadIdx.x;
-        while (bits) {
-          const int e = __ffs(bits) - 1;
-          bits &= bits - 1u;
-          const uint32_t k = unit_key(raw[r][h], e);
-          if (pos < (unsigned)kCandCTA)
-            cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
-          ++pos;
-          if (hist[r]) {
-            const uint32_t bin = k16m[r] - (k >> 16);
-            if (bin < (uint32_t)kWalkBins) atomicAdd(&hist[r][bin], 1u);
-          }
+        const uint32_t k = unit_key(v, e);
+        if (pos < (unsigned)kCandCTA)
+          cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+        ++pos;
+        if (hist[r]) {
+          const uint32_t bin = k16m[r] - (k >> 16);
+          if (bin < (uint32_t)kWalkBins) red_add_shared(&hist[r][bin], 1u);
         }
       }
     }
@@ -1899,8 +1905,8 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
                           : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
     }
     // members at or above the threshold, inserted; those past the list's end kept
-    // in drop[r][h] (register bits) for after the threshold rises
-    uint32_t drop[2][kWinUnits];
+    // in drop[r] (bit 8 h + e of unit h's element e) for after the threshold rises
+    uint32_t drop[2] = {0u, 0u};
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       // the threshold key's value rounded up to bf16: a bf16 logit reaches the key
@@ -1913,24 +1919,24 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
       for (int h = 0; h < kWinUnits; ++h) {
         const uint32_t m = (r < nrows && !fail[r]) ? unit_ge_bits(raw[r][h], t2) : 0u;
         mb[h] = m;
-        drop[r][h] = 0u;
         cnt += __popc(m);
       }
-      if (!__any_sync(kFull, cnt != 0u)) continue;
-      unsigned pos = warp_reserve(&sh.ncand[r], cnt);
+      if (!cnt) continue;
+      unsigned pos = atomicAdd(&sh.ncand[r], cnt);
+      uint32_t bits = 0u;
 #pragma unroll
-      for (int h = 0; h < kWinUnits; ++h) {
-        uint32_t bits = mb[h];
+      for (int h = 0; h < kWinUnits; ++h) bits |= mb[h] << (8 * h);
+      while (bits) {
+        const int t = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int h = t >> 3, e = t & 7;
+        const uint4 v = h == 0 ? raw[r][0] : h == 1 ? raw[r][1] : h == 2 ? raw[r][2] : raw[r][3];
         const int u = tail ? full : base + h * CT + (int)threadIdx.x;
-        while (bits) {
-          const int e = __ffs(bits) - 1;
-          bits &= bits - 1u;
-          if (pos < (unsigned)kCandCTA)
-            list[r][pos] = ((uint64_t)unit_key(raw[r][h], e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
-          else
-            drop[r][h] |= 1u << e;
-          ++pos;
-        }
+        if (pos < (unsigned)kCandCTA)
+          list[r][pos] = ((uint64_t)unit_key(v, e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+        else
+          drop[r] |= 1u << t;
+        ++pos;
       }
     }
     // the list sizes, read by every thread between two barriers (the next round's
@@ -1960,38 +1966,26 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
           return u < ubf ? __ldg(reinterpret_cast<const uint4*>(rows[r]) + u)
                          : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
         };
-#pragma unroll
-        for (int h = 0; h < kWinUnits; ++h) {
-          uint32_t bits = drop[r][h], keep = 0u;
-          if (bits) {
-            const uint4 v = unit(h);
-            while (bits) {
-              const int e = __ffs(bits) - 1;
-              bits &= bits - 1u;
-              if (unit_key(v, e) >= thr) keep |= 1u << e;
-            }
-          }
-          drop[r][h] = keep;
-          cnt += __popc(keep);
+        uint32_t keep = 0u;
+        for (uint32_t bits = drop[r]; bits; bits &= bits - 1u) {
+          const int t = __ffs(bits) - 1;
+          if (unit_key(unit(t >> 3), t & 7) >= thr) keep |= 1u << t;
         }
-        unsigned pos = warp_reserve(&sh.ncand[r], cnt);
-#pragma unroll
-        for (int h = 0; h < kWinUnits; ++h) {
-          uint32_t bits = drop[r][h], left = 0u;
-          if (!bits) continue;
-          const uint4 v = unit(h);
+        drop[r] = keep;
+        cnt = __popc(keep);
+        unsigned pos = cnt ? atomicAdd(&sh.ncand[r], cnt) : 0u;
+        uint32_t left = 0u;
+        for (uint32_t bits = drop[r]; bits; bits &= bits - 1u) {
+          const int t = __ffs(bits) - 1;
+          const int h = t >> 3, e = t & 7;
           const int u = tail ? full : base + h * CT + (int)threadIdx.x;
-          while (bits) {
-            const int e = __ffs(bits) - 1;
-            bits &= bits - 1u;
-            if (pos < (unsigned)kCandCTA)
-              list[r][pos] = ((uint64_t)unit_key(v, e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
-            else
-              left |= 1u << e;
-            ++pos;
-          }
-          drop[r][h] = left;
+          if (pos < (unsigned)kCandCTA)
+            list[r][pos] = ((uint64_t)unit_key(unit(h), e) << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
+          else
+            left |= 1u << t;
+          ++pos;
         }
+        drop[r] = left;
         __syncthreads();
         n = sh.ncand[r];
         if (n <= (unsigned)kCandCTA) break;

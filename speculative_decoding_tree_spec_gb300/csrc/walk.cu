@@ -1098,18 +1098,30 @@ __device__ bool window_collect_fast(const void* const (&rows)[2], int nrows, int
         const uint4 v = h == 0 ? raw[r][0] : h == 1 ? raw[r][1] : h == 2 ? raw[r][2] : raw[r][3];
         const int u = tail ? full : base + h * CT + (int)threadIdx.x;
         const uint32_t k = unit_key(v, e);
-        if (pos < (unsigned)kCandCTA)
+        if (pos < (unsigned)kCandCTA) {
           cand[r][pos] = ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)(u * 8 + e));
-        ++pos;
-        if (hist[r]) {
+        } else if (hist[r]) {
+          // a member past the list is counted here; listed ones after the pass
           const uint32_t bin = k16m[r] - (k >> 16);
           if (bin < (uint32_t)kWalkBins) red_add_shared(&hist[r][bin], 1u);
         }
+        ++pos;
       }
     }
   }
-  win_stage_end(stg, sh, stop);
-  return stop == INT_MAX;
+  win_stage_end(stg, sh, stop);  // ends with a barrier: the lists are complete
+  if (stop != INT_MAX) return false;
+  // the listed members' key counts, every thread over its share of the lists
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r >= nrows || !hist[r]) continue;
+    const unsigned n = min(sh.ncand[r], (unsigned)kCandCTA);
+    for (unsigned i = threadIdx.x; i < n; i += CT) {
+      const uint32_t bin = k16m[r] - (uint32_t)(cand[r][i] >> 48);
+      if (bin < (uint32_t)kWalkBins) red_add_shared(&hist[r][bin], 1u);
+    }
+  }
+  return true;
 }
 
 // Step 2 after the sort: the cut from n sorted candidates (descending, padded to
@@ -1905,8 +1917,10 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
                           : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2);
     }
     // members at or above the threshold, inserted; those past the list's end kept
-    // in drop[r] (bit 8 h + e of unit h's element e) for after the threshold rises
+    // in drop[r] (bit 8 h + e of unit h's element e) for after the threshold rises;
+    // end[r]: the end of this thread's slots (0 if it took none)
     uint32_t drop[2] = {0u, 0u};
+    unsigned end[2] = {0u, 0u};
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       // the threshold key's value rounded up to bf16: a bf16 logit reaches the key
@@ -1923,6 +1937,7 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
       }
       if (!cnt) continue;
       unsigned pos = atomicAdd(&sh.ncand[r], cnt);
+      end[r] = pos + cnt;
       uint32_t bits = 0u;
 #pragma unroll
       for (int h = 0; h < kWinUnits; ++h) bits |= mb[h] << (8 * h);
@@ -1939,15 +1954,15 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
         ++pos;
       }
     }
-    // the list sizes, read by every thread between two barriers (the next round's
-    // reservations may not start before all have read them)
-    __syncthreads();
-    const unsigned n_end[2] = {sh.ncand[0], sh.ncand[1]};
-    __syncthreads();
+    // whether a list passed half full: the largest slot end any thread took is the list
+    // size, so one barrier reduction decides it for the block; only then is the size
+    // read (nothing changes it before the compaction's own barriers)
+    const int busy = __syncthreads_or((end[0] > (unsigned)kCandCTA / 2) ||
+                                      (end[1] > (unsigned)kCandCTA / 2));
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      if (r >= nrows || fail[r]) continue;
-      unsigned n = n_end[r];
+      if (!busy || r >= nrows || fail[r]) continue;
+      unsigned n = sh.ncand[r];
       if (n <= (unsigned)kCandCTA) {
         if (n > (unsigned)kCandCTA / 2) tk_compact(list[r], n, K, hist[r], sh, r);
         continue;
@@ -1993,6 +2008,8 @@ __device__ bool tk_collect(const void* const (&rows)[2], int nrows, int V, int u
       if (fail[r] && threadIdx.x == 0) sh.ncand[r] = 0u;
       __syncthreads();
     }
+    // every thread has read the sizes before the next round reserves slots
+    if (busy) __syncthreads();
   }
   win_stage_end(stg, sh, stop);
   return stop == INT_MAX;

@@ -523,14 +523,14 @@ struct CShared {
   int sc_ok[2], sc_bin[2];
   unsigned sc_j[2], sc_kept[2], sc_ncut[2];
   unsigned long long sc_sf[2];
-  unsigned tie_cnt[2], mem_n[2];
+  unsigned mem_n[2];
   // accept-test inputs of the first kPreKids children of the current node: the
   // unnormalised fp64 weights of the drafted token under p and q, its order keys,
   // and its accept uniform
   double kid_e[2][kPreKids];
   uint32_t kid_k[2][kPreKids];
   double kid_u[kPreKids];
-  int tie_max[2], tie_idx[2];
+  int tie_idx[2];
   // visited-rows-only schedule: per-warp row statistics of the cluster's stats pass
   float st_m[2][CW];
   double st_s[2][CW];
@@ -1588,7 +1588,6 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
     else if ((threadIdx.x & 31) == 0)
       sh.sc_ok[warp] = 0;
   }
-  if (threadIdx.x < 2) { sh.tie_cnt[threadIdx.x] = 0u; sh.tie_max[threadIdx.x] = -1; }
   __syncthreads();
   bool ok[2] = {false, false};
 #pragma unroll
@@ -1596,66 +1595,44 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
     if (r < nrows) ok[r] = sh.sc_ok[r] != 0;
   uint32_t cut32[2] = {0u, 0u};
   if (ok[0] || ok[1]) {
-    // members of the cut key in this CTA's candidate list
+    // Each CTA's number of members of the cut key is its own count of that key, read
+    // from its histogram through distributed shared memory (every histogram stays as
+    // it is until all CTAs have passed the exchange below).  The cut index is the
+    // largest member when the whole group is kept, else the j-th member in index
+    // order; either way one CTA (the owner) holds it.
+    int owner[2] = {-1, -1};
+    unsigned jr[2] = {0u, 0u};
+    bool want_max[2] = {false, false};
+    int cut_idx[2] = {0, 0};
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;
       if (!ok[r]) continue;
       cut32[r] = key_from16(k16m[r] - (uint32_t)sh.sc_bin[r]);
-      if (own_over[r]) {
-        for (int u = ua + threadIdx.x; u < ub; u += CT) {
-          float z[8];
-          Elt<uint16_t>::unpack(load_raw<uint16_t>(rows[r], V, u), z);
+      unsigned cnt[kMaxC];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (order_key(z[e]) == cut32[r]) {
-              atomicAdd(&sh.tie_cnt[r], 1u);
-              atomicMax(&sh.tie_max[r], u * 8 + e);
-            }
-        }
-      } else {
-        for (unsigned i = threadIdx.x; i < own_n[r]; i += CT) {
-          const uint64_t e = cl[r][i];
-          if ((uint32_t)(e >> 32) == cut32[r]) {
-            atomicAdd(&sh.tie_cnt[r], 1u);
-            atomicMax(&sh.tie_max[r], (int)(~(uint32_t)e));
-          }
-        }
-      }
-    }
-    __syncthreads();
-    uint64_t tw[2];
-    for (int r = 0; r < 2; ++r)
-      tw[r] = (uint64_t)sh.tie_cnt[r] | ((uint64_t)(uint32_t)sh.tie_max[r] << 32);
-    const SlotRow* ts = cluster_share(tw, 2, sh, C, rank, n_ex);
-    if (!ts) return false;
-    // the cut index: the largest member when the whole group is kept, else the
-    // j-th member in index order, found by the CTA whose slice holds it
-    int owner[2] = {-1, -1};
-    unsigned jr[2] = {0u, 0u};
-    int cut_idx[2] = {0, 0};
-    bool need = false;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (r >= nrows) break;
-      if (!ok[r]) continue;
+      for (int q = 0; q < kMaxC; ++q)
+        cnt[q] = q < C ? ld_peer_u32(peer_addr(hist[r] + sh.sc_bin[r], q)) : 0u;
       if (sh.sc_j[r] == sh.sc_ncut[r]) {
-        int mx = -1;
-        for (int q = 0; q < C; ++q) mx = max(mx, (int)(uint32_t)(ts[q][r] >> 32));
-        cut_idx[r] = mx;
+        want_max[r] = true;
+#pragma unroll
+        for (int q = 0; q < kMaxC; ++q)
+          if (q < C && cnt[q]) owner[r] = q;  // the last CTA with a member
       } else {
         unsigned before = 0;
-        for (int q = 0; q < C; ++q) {
-          const unsigned n = (unsigned)ts[q][r];
-          if (owner[r] < 0 && before + n >= sh.sc_j[r]) { owner[r] = q; jr[r] = sh.sc_j[r] - before; }
-          before += n;
+#pragma unroll
+        for (int q = 0; q < kMaxC; ++q) {
+          if (q < C && owner[r] < 0 && before + cnt[q] >= sh.sc_j[r]) {
+            owner[r] = q;
+            jr[r] = sh.sc_j[r] - before;
+          }
+          before += cnt[q];
         }
-        need = true;
       }
     }
+    const bool need = owner[0] >= 0 || owner[1] >= 0;
     if (need) {
-      // every CTA finished reading the histograms before the tie exchange; the
-      // merged counts are no longer needed and hold the owner's member indices
+      // the merged counts are no longer needed and hold the owner's member indices
       if (threadIdx.x < 2) { sh.mem_n[threadIdx.x] = 0u; sh.tie_idx[threadIdx.x] = -1; }
       __syncthreads();
 #pragma unroll
@@ -1692,6 +1669,10 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
         if (owner[r] != (int)rank) continue;
         const unsigned nm = sh.mem_n[r];
         if (nm > (unsigned)kWalkBins) continue;  // tie_idx stays -1: the exact selection decides
+        if (want_max[r]) {
+          for (unsigned i = threadIdx.x; i < nm; i += CT) atomicMax(&sh.tie_idx[r], (int)merged[r][i]);
+          continue;
+        }
         for (unsigned i = threadIdx.x; i < nm; i += CT) {
           const unsigned me = merged[r][i];
           unsigned rk = 0;
@@ -1713,6 +1694,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
         if (cut_idx[r] < 0) ok[r] = false;  // too many tied members: exact selection
       }
     }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (r < nrows && ok[r] && owner[r] < 0) ok[r] = false;  // no member found: exact selection
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if (r >= nrows) break;

@@ -41,7 +41,7 @@ constexpr int kSortW = 2048;   // largest window (per row) the walk resolves by 
 constexpr int kSortPer = kSortW / CT;
 constexpr int kWalkBins = 1024;
 constexpr int kWalkCtasPerSm = 2;  // resident sampling-walk CTAs per SM (register budget)
-constexpr int kPreKids = 16;   // children whose accept-test inputs are prepared in parallel  // bf16: one bin per key in the window below the row maximum
+constexpr int kPreKids = 16;   // children whose accept-test inputs are prepared in parallel
 static_assert(CT == kSelThreads, "the exact selection runs on one walk CTA");
 
 __device__ __forceinline__ const void* row_at(const void* base, const TreeJob& j, int b, int n,
@@ -542,6 +542,9 @@ struct CShared {
   unsigned kp_n;    // this CTA's kept tokens of p (kept-set mode)
   unsigned long long ured[CW];
   int kp_tok;
+  // fp64 reciprocals (GB300's fp64 divide is slow: each is taken once): 1 / T of the
+  // tree, 1 / s_f of the node's p and q rows
+  double inv_td, inv_s64[2];
   // window-pass staging: the two stages' barriers, rounds staged so far
   uint64_t wbar[2];
   uint32_t win_g;
@@ -2384,8 +2387,9 @@ __device__ void build_kept(const TreeJob& job, const uint64_t* list_p, unsigned 
 // Residual mass over the kept set: every CTA's exact fixed-point sum of
 // max(0, p - q) over its tokens, summed over the cluster in rank order; then
 // p <- max(0, p - q) / Z where Z > 0 (the step residual_chain applies per token).
+// rz[j] receives 1 / Z in fp64 (0 when Z == 0), invz[j] the same in fp32 (-1).
 // Returns false if the exchange gave up.
-__device__ bool kept_residual(const KeptSet& ks, unsigned nk, double* Z, float* invz, int j,
+__device__ bool kept_residual(const KeptSet& ks, unsigned nk, double* rz, float* invz, int j,
                               CShared& sh, int C, uint32_t rank, uint32_t& n_ex) {
   unsigned long long part = 0;
   for (unsigned i = threadIdx.x; i < nk; i += CT)
@@ -2395,8 +2399,9 @@ __device__ bool kept_residual(const KeptSet& ks, unsigned nk, double* Z, float* 
   if (!cluster_sum((double)part, sh, C, rank, n_ex, tot, nullptr)) return false;
   const double z = tot * (1.0 / 4398046511104.0);
   if (threadIdx.x == 0) {
-    Z[j] = z;
-    invz[j] = (z > 0.0) ? (float)(1.0 / z) : -1.f;
+    const double r = z > 0.0 ? 1.0 / z : 0.0;
+    rz[j] = r;
+    invz[j] = z > 0.0 ? (float)r : -1.f;
   }
   __syncthreads();
   const float iz = invz[j];
@@ -2505,8 +2510,9 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   const int b = blockIdx.x / C;
   const int N = job.N, V = job.V, W = job.W;
   int32_t *par = tsm, *tok = tsm + N, *cs = tsm + 2 * N, *cl = tsm + 3 * N + 1;
-  double* Z = reinterpret_cast<double*>(tsm + ((4 * N + 1 + 1) & ~1));
-  float* invz = reinterpret_cast<float*>(Z + N);
+  // per residual step j: 1 / Z_j in fp64 (0 when Z_j == 0) and in fp32 (-1 then)
+  double* rz = reinterpret_cast<double*>(tsm + ((4 * N + 1 + 1) & ~1));
+  float* invz = reinterpret_cast<float*>(rz + N);
   float* steps = invz + N;
   // the top-k / top-p cut's buffers (16-byte aligned)
   unsigned char* cut_smem = reinterpret_cast<unsigned char*>(
@@ -2516,7 +2522,10 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
   int status = SPEC_TREE_OK;
   {
     const Samp s0 = tree_samp(job, b, status);
-    if (threadIdx.x == 0) sh.smp = s0;
+    if (threadIdx.x == 0) {
+      sh.smp = s0;
+      sh.inv_td = s0.temperature > 0.0f ? 1.0 / (double)s0.temperature : 0.0;
+    }
   }
   // read from shared memory where used (kept out of the registers)
   const Samp& smp = sh.smp;
@@ -2608,7 +2617,7 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       const int i = (int)threadIdx.x % n_pre, r = (int)threadIdx.x / n_pre;
       const int ch = cl[c0 + i];
       const float z = Elt<T>::at(r ? qrow : prow, tok[ch]);
-      sh.kid_e[r][i] = exp(((double)z - (double)(r ? sq.m : sp.m)) / Td);
+      sh.kid_e[r][i] = exp(((double)z - (double)(r ? sq.m : sp.m)) * sh.inv_td);
       sh.kid_k[r][i] = order_key(z);
       if (r == 0) sh.kid_u[i] = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
     }
@@ -2624,8 +2633,10 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       }
     }
     if (threadIdx.x == 0) {
-      sh.inv_sp = (float)(1.0 / sp.s_f);
-      sh.inv_sq = (float)(1.0 / sq.s_f);
+      sh.inv_s64[0] = 1.0 / sp.s_f;
+      sh.inv_s64[1] = c1 > c0 ? 1.0 / sq.s_f : 0.0;
+      sh.inv_sp = (float)sh.inv_s64[0];
+      sh.inv_sq = (float)sh.inv_s64[1];
     }
     __syncthreads();
     const RowF fp = make_rowf(sp, c, sh.inv_sp), fq = make_rowf(sq, c, sh.inv_sq);
@@ -2643,8 +2654,8 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
         double P, Q, uu;
         if (i - c0 < kPreKids) {
           const int k = i - c0;
-          P = kept_key(sh.kid_k[0][k], x, sp) ? sh.kid_e[0][k] / sp.s_f : 0.0;
-          Q = kept_key(sh.kid_k[1][k], x, sq) ? sh.kid_e[1][k] / sq.s_f : 0.0;
+          P = kept_key(sh.kid_k[0][k], x, sp) ? sh.kid_e[0][k] * sh.inv_s64[0] : 0.0;
+          Q = kept_key(sh.kid_k[1][k], x, sq) ? sh.kid_e[1][k] * sh.inv_s64[1] : 0.0;
           uu = sh.kid_u[k];
         } else {
           P = prob64<T>(prow, x, sp, Td);
@@ -2652,17 +2663,30 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
           uu = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
         }
         for (int r = 0; r < j; ++r)
-          if (Z[r] > 0.0) P = fmax(0.0, P - Q) / Z[r];
-        const double alpha = (Q > 0.0) ? fmin(1.0, P / Q) : (P > 0.0 ? 1.0 : 0.0);
-        if (lead && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = (float)alpha;
-        sh.accept = (uu <= alpha);
+          if (rz[r] > 0.0) P = fmax(0.0, P - Q) * rz[r];
+        // accept iff uu <= min(1, P / Q), tested as uu * Q <= P (no fp64 divide); the
+        // reported alpha is divided in fp32 where both lie in its normal range
+        bool accept;
+        if (Q > 0.0) {
+          accept = P >= Q || uu * Q <= P;
+          if (lead && job.out_alpha) {
+            float a = 1.0f;
+            if (P < Q)
+              a = (P > 1e-30 && Q > 1e-30) ? (float)P / (float)Q : (float)(P / Q);
+            job.out_alpha[(int64_t)b * N + ch] = a;
+          }
+        } else {
+          accept = P > 0.0;
+          if (lead && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = accept ? 1.0f : 0.0f;
+        }
+        sh.accept = accept;
       }
       __syncthreads();
       const int acc = sh.accept;
       __syncthreads();
       if (acc) { next = ch; break; }
       if (p_listed) {
-        if (!kept_residual(ks, sh.kp_n, Z, invz, j, sh, C, rank, n_ex)) { timed_out = true; break; }
+        if (!kept_residual(ks, sh.kp_n, rz, invz, j, sh, C, rank, n_ex)) { timed_out = true; break; }
         if (lead && threadIdx.x == 0 && job.counters) atomicAdd(&job.counters[3], 1ull);
         ++j;
         continue;
@@ -2672,8 +2696,9 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       double z;
       if (!cluster_sum(part, sh, C, rank, n_ex, z, nullptr)) { timed_out = true; break; }
       if (threadIdx.x == 0) {
-        Z[j] = z;
-        invz[j] = (z > 0.0) ? (float)(1.0 / z) : -1.f;
+        const double r = z > 0.0 ? 1.0 / z : 0.0;
+        rz[j] = r;
+        invz[j] = z > 0.0 ? (float)r : -1.f;
         if (lead && job.counters) {
           atomicAdd(&job.counters[2], 2ull * (unsigned long long)V * Elt<T>::kBytes);
           atomicAdd(&job.counters[3], 1ull);

@@ -169,13 +169,15 @@ int verify_impl(uint32_t phases, const void* logits_p, const void* logits_q, spe
   rj.counters = tj.counters;
   rj.req_temperature = req_temperature;
   const int virtual_rows = B * N * (greedy ? 1 : 2);
-  // the visited-rows-only schedule has no dense pass
-  if ((phases & SPEC_PHASE_ROWS) && !tj.visited_only &&
+  // small vocabularies without a cut: one warp per tree reads the rows it visits
+  const bool small = small_walk_applies(tj, greedy, params.flags);
+  // the visited-rows-only schedule and the small-vocabulary walk have no dense pass
+  if ((phases & SPEC_PHASE_ROWS) && !tj.visited_only && !small &&
       launch_row_pass(rj, dtype, virtual_rows, s) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   if (phases & SPEC_PHASE_WALK) {
-    if (launch_tree_walk(tj, dtype, greedy, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_tree_walk(tj, dtype, greedy, small, s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (out_counters &&
         cudaMemcpyAsync(out_counters, counters, sizeof(spec_verify_counters),
                         cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -361,7 +363,7 @@ extern "C" int spec_verify_tree_fused_lmhead_phases(
   tj.out_status = out_status;
   tj.counters = cnt;
   if (phases & SPEC_PHASE_WALK) {
-    if (launch_tree_walk(tj, SPEC_BF16, greedy, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_tree_walk(tj, SPEC_BF16, greedy, false, s) != cudaSuccess) return SPEC_ERR_CUDA;
     if (out_counters && cudaMemcpyAsync(out_counters, counters, sizeof(spec_verify_counters),
                                         cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return SPEC_ERR_CUDA;

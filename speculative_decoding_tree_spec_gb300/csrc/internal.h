@@ -120,7 +120,11 @@ struct TreeJob {
 
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_row_pass(const RowJob& job, spec_dtype dtype, int num_rows, cudaStream_t s);
-cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, cudaStream_t s);
+// Small vocabularies without a cut: one warp per tree computes its visited rows'
+// statistics itself (no dense pass precedes it).
+bool small_walk_applies(const TreeJob& job, bool greedy, uint32_t flags);
+cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, bool small,
+                             cudaStream_t s);
 cudaError_t launch_philox_words(uint64_t seed, uint64_t offset, const int32_t* b_idx,
                                 const int32_t* node_idx, int32_t n, uint32_t* out,
                                 cudaStream_t s);

@@ -388,6 +388,10 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
     fence_barrier_init();
   }
   __syncthreads();
+  // a kernel launched after this one with programmatic stream serialization (the tree
+  // walk) may be scheduled now; it waits for this grid's completion before reading
+  // anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   // the balanced schedule (modes 0 and 2 and list launches: every G-th virtual row)
   const bool sched = use_schedule(job, MODE, (int)gridDim.x);
   int* const sched_rows = reinterpret_cast<int*>(

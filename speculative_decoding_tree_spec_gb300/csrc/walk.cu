@@ -2550,6 +2550,9 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     const int st = load_tree(job, b, par, tok, cs, cl, lead, &sh.status);
     if (status == SPEC_TREE_OK) status = st;
   }
+  // the kernel launched before this one in the stream (the dense pass) has completed
+  // and its writes are visible after this point (returns at once without one)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int nunits = (V + E - 1) / E;
   const int ua = (int)((int64_t)nunits * rank / C), ub = (int)((int64_t)nunits * (rank + 1) / C);
   int32_t* out_tok = job.out_tokens + (int64_t)b * W;
@@ -2776,6 +2779,207 @@ cudaError_t launch_greedy(const TreeJob& job, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Small vocabularies (V <= kSmallMaxV) without a top-k / top-p cut: one warp per
+// tree computes everything itself.  A row is eight logits per lane at most, so the
+// statistics, the accept tests, the residuals and the final draw are warp
+// reductions over registers, and no dense pass precedes the walk (a tree reads only
+// the rows it visits).  The rules are the cluster walk's: children in node order,
+// accept iff u <= min(1, P/Q) (Q = 0: iff P > 0), p <- max(0, p - q) / Z after a
+// rejection (unchanged when Z = 0), the final token the smallest index whose
+// inclusive prefix reaches r times the total; probabilities in fp64 (a row is at
+// most kSmallPer values per lane).
+// ---------------------------------------------------------------------------
+constexpr int kSmallMaxV = 256;
+constexpr int kSmallPer = kSmallMaxV / 32;  // logits per lane
+constexpr int kSmallMaxN = 64;
+constexpr int kSmallWarps = 4;              // trees per block
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Tempered probabilities of one row into pr[] (fp64, as the oracle takes them; slots
+// past V hold 0); status of the row (SPEC_ROW_NONFINITE for NaN, +inf or all -inf)
+// and its argmax.
+template <typename T>
+__device__ int small_row(const void* row, int V, double inv_t, double (&pr)[kSmallPer],
+                         int& argmax) {
+  const int lane = threadIdx.x & 31;
+  float z[kSmallPer];
+  int bad = 0;
+  float m = -CUDART_INF_F;
+#pragma unroll
+  for (int k = 0; k < kSmallPer; ++k) {
+    const int i = k * 32 + lane;
+    z[k] = i < V ? Elt<T>::at(row, i) : -CUDART_INF_F;
+    bad |= (z[k] != z[k]) || (z[k] == CUDART_INF_F);
+    m = fmaxf(m, z[k]);
+  }
+  m = warp_max(m);
+  bad = __any_sync(kFull, bad) || m == -CUDART_INF_F;
+  int idx = INT_MAX;
+#pragma unroll
+  for (int k = kSmallPer - 1; k >= 0; --k)
+    if (z[k] == m && k * 32 + lane < V) idx = k * 32 + lane;
+  argmax = warp_min_i(idx);
+  if (bad) return SPEC_ROW_NONFINITE;
+  double s = 0.0;
+#pragma unroll
+  for (int k = 0; k < kSmallPer; ++k) {
+    pr[k] = 0.0;
+    if (k * 32 < V && z[k] != -CUDART_INF_F) pr[k] = exp(((double)z[k] - (double)m) * inv_t);
+    s += pr[k];
+  }
+  const double inv_s = 1.0 / warp_sum_d(s);
+#pragma unroll
+  for (int k = 0; k < kSmallPer; ++k) pr[k] *= inv_s;
+  return SPEC_TREE_OK;
+}
+
+// Element x of a lane-strided fp64 row held in registers (lane x % 32, slot x / 32).
+__device__ __forceinline__ double small_at(const double (&a)[kSmallPer], int x) {
+  double v = 0.0;
+#pragma unroll
+  for (int k = 0; k < kSmallPer; ++k)
+    if (k == (x >> 5)) v = a[k];
+  return __shfl_sync(kFull, v, x & 31);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kSmallWarps) small_walk_kernel(TreeJob job) {
+  __shared__ int32_t s_par[kSmallWarps][kSmallMaxN];
+  __shared__ int32_t s_tok[kSmallWarps][kSmallMaxN];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kSmallWarps + w;
+  if (b >= job.B) return;  // the whole warp: nothing below synchronises the block
+  const int N = job.N, V = job.V, W = job.W;
+  int32_t* par = s_par[w];
+  int32_t* tok = s_tok[w];
+  for (int n = lane; n < N; n += 32) {
+    par[n] = job.parents[(int64_t)b * N + n];
+    tok[n] = job.tokens[(int64_t)b * N + n];
+    if (job.out_alpha) job.out_alpha[(int64_t)b * N + n] = __int_as_float(0x7fc00000);
+  }
+  __syncwarp();
+  // the tree checks of load_tree: root first, parents before children, tokens in the
+  // vocabulary, no node deeper than max_depth
+  int bad = 0;
+  for (int n = lane; n < N; n += 32)
+    bad |= n == 0 ? (par[0] != -1) : (par[n] < 0 || par[n] >= n || tok[n] < 0 || tok[n] >= V);
+  bad = __any_sync(kFull, bad);
+  if (!bad) {
+    for (int n = lane; n < N; n += 32) {
+      int x = n, d = 0;
+      while (x != 0 && d < W) { x = par[x]; ++d; }
+      bad |= (x != 0 || d > W - 1);
+    }
+    bad = __any_sync(kFull, bad);
+  }
+  int status = bad ? SPEC_TREE_INVALID : SPEC_TREE_OK;
+  int32_t* out_tok = job.out_tokens + (int64_t)b * W;
+  int32_t* out_path = job.out_path + (int64_t)b * W;
+  const double inv_t = 1.0 / (double)job.temperature;
+  const size_t eb = Elt<T>::kBytes;
+  int u = 0, n_acc = 0, final_tok = -1;
+  double P[kSmallPer], Q[kSmallPer];
+  while (status == SPEC_TREE_OK) {
+    int argmax_p = 0, argmax_q = 0;
+    status = small_row<T>(row_at(job.base_p, job, b, u, eb), V, inv_t, P, argmax_p);
+    if (status != SPEC_TREE_OK) break;
+    bool has_child = false;
+    for (int n = u + 1 + lane; n < N; n += 32) has_child |= (par[n] == u);
+    has_child = __any_sync(kFull, has_child);
+    if (has_child) {
+      status = small_row<T>(row_at(job.base_q, job, b, u, eb), V, inv_t, Q, argmax_q);
+      if (status != SPEC_TREE_OK) break;
+    }
+    if (lane == 0 && job.counters)
+      atomicAdd(&job.counters[2], (unsigned long long)(has_child ? 2 : 1) * V * eb);
+    int next = -1;
+    for (int ch = u + 1; has_child && ch < N; ++ch) {
+      if (par[ch] != u) continue;
+      const int x = tok[ch];
+      const double px = small_at(P, x), qx = small_at(Q, x);
+      const double uu = unit_uniform(philox_words(job.seed, job.offset, b, ch).x);
+      bool accept;
+      float alpha;
+      if (qx > 0.0) {
+        accept = px >= qx || uu * qx <= px;
+        alpha = px >= qx ? 1.0f
+                         : ((px > 1e-30 && qx > 1e-30) ? (float)px / (float)qx : (float)(px / qx));
+      } else {
+        accept = px > 0.0;
+        alpha = accept ? 1.0f : 0.0f;
+      }
+      if (lane == 0 && job.out_alpha) job.out_alpha[(int64_t)b * N + ch] = alpha;
+      if (accept) { next = ch; break; }
+      // rejected: p <- max(0, p - q) / Z (unchanged when Z == 0)
+      double part = 0.0;
+#pragma unroll
+      for (int k = 0; k < kSmallPer; ++k) part += fmax(0.0, P[k] - Q[k]);
+      const double z = warp_sum_d(part);
+      if (z > 0.0) {
+        const double iz = 1.0 / z;
+#pragma unroll
+        for (int k = 0; k < kSmallPer; ++k) P[k] = fmax(0.0, P[k] - Q[k]) * iz;
+      }
+      if (lane == 0 && job.counters) atomicAdd(&job.counters[3], 1ull);
+    }
+    if (next >= 0) {
+      if (lane == 0) {
+        out_tok[n_acc] = tok[next];
+        out_path[n_acc + 1] = next;
+      }
+      ++n_acc;
+      u = next;
+      continue;
+    }
+    // the final draw from p: the smallest index whose inclusive prefix reaches r times
+    // the total (index order: slot-major, lanes within a slot)
+    const double r = unit_uniform(philox_words(job.seed, job.offset, b, u).y);
+    double mine = 0.0;
+#pragma unroll
+    for (int k = 0; k < kSmallPer; ++k) mine += P[k];
+    const double total = warp_sum_d(mine);
+    int tokx = -1, last = -1;
+    if (total > 0.0) {
+      const double t = r * total;
+      double run = 0.0;
+#pragma unroll
+      for (int k = 0; k < kSmallPer; ++k) {
+        if (k * 32 >= V) break;
+        double incl = P[k];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double v = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += v;
+        }
+        incl += run;
+        const unsigned hit = __ballot_sync(kFull, P[k] > 0.0 && incl >= t);
+        const unsigned any = __ballot_sync(kFull, P[k] > 0.0);
+        if (any) last = k * 32 + 31 - __clz(any);
+        if (hit && tokx < 0) tokx = k * 32 + __ffs(hit) - 1;
+        run = __shfl_sync(kFull, incl, 31);
+      }
+      if (tokx < 0) tokx = last;  // r == 1 under rounding: the last token with mass
+    }
+    final_tok = tokx >= 0 ? tokx : argmax_p;
+    if (lane == 0 && job.counters) atomicAdd(&job.counters[4], 1ull);
+    break;
+  }
+  if (lane == 0) finish_tree(job, b, status, n_acc, final_tok, true);
+}
+
+template <typename T>
+cudaError_t launch_small(const TreeJob& job, cudaStream_t s) {
+  const int grid = (job.B + kSmallWarps - 1) / kSmallWarps;
+  small_walk_kernel<T><<<grid, 32 * kSmallWarps, 0, s>>>(job);
+  return cudaGetLastError();
+}
+
 int floor_pow2(int x) {
   int p = 1;
   while (p * 2 <= x) p *= 2;
@@ -2823,19 +3027,32 @@ cudaError_t launch_sampling(const TreeJob& job, cudaStream_t s) {
   cfg.blockDim = dim3(CT);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the walk's CTAs may start (and load their trees)
+  // while the dense pass before it in the stream finishes; they wait for its
+  // results with griddepcontrol.wait before reading any row statistics
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, cluster_walk_kernel<T>, job, C, max_steps, ring_stages);
 }
 
 }  // namespace
 
-cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, cudaStream_t s) {
+bool small_walk_applies(const TreeJob& job, bool greedy, uint32_t flags) {
+  return !greedy && !job.trunc && !job.req_temperature && job.V <= kSmallMaxV &&
+         job.N <= kSmallMaxN && !(flags & SPEC_FLAG_TEST_STALL);
+}
+
+cudaError_t launch_tree_walk(const TreeJob& job, spec_dtype dtype, bool greedy, bool small,
+                             cudaStream_t s) {
+  if (small)
+    return dtype == SPEC_BF16 ? launch_small<uint16_t>(job, s) : launch_small<float>(job, s);
   if (greedy)
     return dtype == SPEC_BF16 ? launch_greedy<uint16_t>(job, s) : launch_greedy<float>(job, s);
   if (dtype == SPEC_BF16) return launch_sampling<uint16_t>(job, s);

@@ -277,6 +277,18 @@ def test_tree_row_pass_reads_exactly_the_needed_rows(per_request):
     assert (got_q[~need_q] == 0xAB).all()
 
 
+# --- small vocabularies without a cut: one warp per tree, no dense pass --------------
+
+@pytest.mark.parametrize("dtype,V,N", [("f32", 256, 64), ("bf16", 200, 40), ("f32", 33, 12),
+                                       ("bf16", 1, 5), ("f32", 32, 4)])
+def test_small_vocabulary_walk(dtype, V, N):
+    w = W["tree60_b64_v128256"].with_(B=300, N=N, V=V, dtype=dtype, depth=min(6, N - 1),
+                                      temperature=0.9, top_k=0, top_p=1.0)
+    gpu, n, ex, err = _parity(w, seed=51)
+    # the rows it visits are read by the walk itself
+    assert gpu["counters"]["dense_rows"] == 0 and gpu["counters"]["walk_bytes"] > 0
+
+
 # --- the top-k route of bf16 rows (per-CTA lists under a rising threshold) ----------
 
 @pytest.mark.parametrize("w", [

@@ -458,13 +458,18 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     step_bytes = counters["dense_bytes"] + counters["walk_bytes"]
-    if args.visited_only:
-        # no dense pass: the walk is the only kernel; its rows read over its time
+    # no dense pass ran: the visited-rows-only schedule, or a small vocabulary without a
+    # cut (one warp per tree reads the rows it visits)
+    no_dense = args.visited_only or counters["dense_rows"] == 0
+    if no_dense:
+        # the walk is the only kernel; its rows read over its time
         walk_ms = ms_per_step - row_avg_ms
         achieved = counters["walk_bytes"] / (walk_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": None,
-                    "kernel": "cluster_walk_kernel (visited rows only; latency-bound)",
+                    "kernel": ("cluster_walk_kernel (visited rows only; latency-bound)"
+                               if args.visited_only else
+                               "small_walk_kernel (one warp per tree; latency-bound)"),
                     "peak_source": f"{peak_kind} hbm_gbs",
                     "algorithmic_bytes_per_launch": counters["walk_bytes"],
                     "avg_launch_ms": walk_ms}
@@ -507,7 +512,8 @@ def run_ours(args):
                    "tree": f"{w.tree}, depth {inp['max_depth']}, branching <= {w.max_branch}",
                    "rng_offset": "fixed per step",
                    "schedule": ("visited rows only (no dense pass)" if args.visited_only
-                                else "dense pass over every row"),
+                                else "one warp per tree, no dense pass (small vocabulary)"
+                                if no_dense else "dense pass over every row"),
                    "sampling": ("per request: trees cycle through greedy, the workload's "
                                 "setting, top-k 50 at T=1, top-p 0.8 at T=0.5"
                                 if args.per_request else "one setting for every tree"),
@@ -518,7 +524,7 @@ def run_ours(args):
         "step_hbm_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
         "work_per_step": counters,
         "roofline": roofline,
-        "gpu_launches": (1 if args.visited_only else 2) * K,  # [row pass +] walk per step
+        "gpu_launches": (1 if no_dense else 2) * K,  # [dense pass +] walk per call
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     result["clocks"]["warmup_and_timed"] = clocks.summary(t_warm0, t_wall1)

@@ -1388,8 +1388,9 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
 
 
 // bf16 rows: the window's cut from the cluster's merged counts per 16-bit key
-// (bin = K16m - key), scanned by one warp with the dense row pass's crossing rules
-// (top-k count, then the top-p mass target over exact fixed-point weights).
+// (bin = K16m - key) and the keys' fixed-point weights (wbin, filled beforehand),
+// scanned by one warp with the dense row pass's crossing rules (top-k count, then
+// the top-p mass target over exact fixed-point weights).
 // Results in sh.sc_*[r]; sh.sc_ok[r] = 0 when the window cannot decide the cut.
 __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin, int nb,
                                  uint32_t K16m, float m, float c, double s_all,
@@ -1402,9 +1403,7 @@ __device__ void bf16_window_scan(const unsigned* hist, unsigned long long* wbin,
   unsigned lc = 0;
   unsigned long long lw = 0;
   for (int bin = b_lo; bin < b_hi; ++bin) {
-    const unsigned long long wgt =
-        to_fixed(tempered_weight(key_value(key_from16(K16m - (uint32_t)bin)), m, c));
-    wbin[bin] = wgt;
+    const unsigned long long wgt = wbin[bin];  // filled with the merge, every thread a bin
     lc += hist[bin];
     lw += (unsigned long long)hist[bin] * wgt;
   }
@@ -1580,6 +1579,9 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
 #pragma unroll
       for (int q = 0; q < kMaxC; ++q) t += v[q];
       merged[r][i] = t;
+      // the key's weight, for the scan (every thread its bins, not one warp all)
+      wbin[r][i] = to_fixed(tempered_weight(key_value(key_from16(k16m[r] - (uint32_t)i)),
+                                            st[r]->m, c));
     }
   }
   __syncthreads();

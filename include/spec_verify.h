@@ -446,6 +446,20 @@ int spec_tree_build(const int32_t* cand_parent, const int32_t* cand_token,
                     int32_t* out_position_ids, int32_t* out_src, uint8_t* out_mask,
                     int32_t* out_status, spec_stream_t stream);
 
+/*
+ * Checked builds.  The library built with -DSPEC_CHECK (build.py's check variant,
+ * _build/check/libspecverify_check.so) checks the indices of its dense pass's and
+ * walk's buffer accesses on the device; an index out of range sets a bit of that
+ * file's error word and is replaced by 0, so the access stays inside its buffer.
+ * spec_check_errors writes the dense pass's word to out_words[0] and the walk's to
+ * out_words[1] (host memory, 2 words) and clears them; both are 0 when nothing was
+ * caught, and always 0 in the regular build.  It waits for the device.  Returns
+ * SPEC_OK, SPEC_ERR_INVALID_ARG (NULL out_words) or SPEC_ERR_CUDA.
+ * spec_check_build returns 1 in a checked build, else 0.
+ */
+int spec_check_errors(uint32_t* out_words);
+int spec_check_build(void);
+
 /* Static description of a return code (never NULL). */
 const char* spec_error_string(int code);
 

@@ -77,6 +77,10 @@ def lib():
             L = ctypes.CDLL(LIB_PATH)
             P = ctypes.c_void_p
             i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+            L.spec_check_errors.argtypes = [P]
+            L.spec_check_errors.restype = ctypes.c_int
+            L.spec_check_build.argtypes = []
+            L.spec_check_build.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, ctypes.c_int]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_tree.argtypes = [P, P, ctypes.c_int, i32, i32, i32, i64, i64, P, P, i32,
@@ -129,6 +133,16 @@ def lib():
 
 def error_string(code: int) -> str:
     return lib().spec_error_string(int(code)).decode()
+
+
+def check_errors() -> list:
+    """spec_check_errors: the checked build's two device error words (dense pass,
+    walk), read and cleared; [0, 0] in the regular build.  Waits for the device."""
+    words = (ctypes.c_uint32 * 2)()
+    rc = lib().spec_check_errors(ctypes.addressof(words))
+    if rc != 0:
+        raise SpecError(rc, "spec_check_errors")
+    return [int(words[0]), int(words[1])]
 
 
 def params(temperature: float, top_k: int = 0, top_p: float = 1.0, flags: int = 0) -> SamplingParams:

@@ -434,3 +434,19 @@ extern "C" const char* spec_error_string(int code) {
     default: return "unknown error code";
   }
 }
+
+extern "C" int spec_check_errors(uint32_t* out_words) {
+  if (!out_words) return SPEC_ERR_INVALID_ARG;
+  out_words[0] = check_word_rows();
+  out_words[1] = check_word_walk();
+  if (out_words[0] == 0xffffffffu || out_words[1] == 0xffffffffu) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+extern "C" int spec_check_build(void) {
+#ifdef SPEC_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}

@@ -13,6 +13,27 @@ namespace svk {
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------------------
+// Checked builds (compiled with -DSPEC_CHECK): an index found outside its range
+// sets a bit of this translation unit's error word and is replaced by 0, so the
+// access stays inside its buffer; spec_check_errors() reads and clears the words.
+// Other builds compile the checks to nothing.
+// ---------------------------------------------------------------------------
+#ifdef SPEC_CHECK
+static __device__ unsigned int g_spec_check;
+#define SPEC_CHECK_INDEX(i, n, bit)                                                    \
+  do {                                                                                 \
+    if ((unsigned long long)(long long)(i) >= (unsigned long long)(long long)(n)) {    \
+      atomicOr(&::svk::g_spec_check, 1u << (bit));                                     \
+      (i) = 0;                                                                         \
+    }                                                                                  \
+  } while (0)
+#else
+#define SPEC_CHECK_INDEX(i, n, bit) \
+  do {                              \
+  } while (0)
+#endif
+
+// ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
 // as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies, the key advanced
 // by the golden-ratio / sqrt(3) Weyl increments between rounds.

@@ -120,6 +120,9 @@ struct TreeJob {
 
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_row_pass(const RowJob& job, spec_dtype dtype, int num_rows, cudaStream_t s);
+// Checked builds (-DSPEC_CHECK): each file's device error word, read and cleared.
+uint32_t check_word_rows();
+uint32_t check_word_walk();
 // Small vocabularies without a cut: one warp per tree computes its visited rows'
 // statistics itself (no dense pass precedes it).
 bool small_walk_applies(const TreeJob& job, bool greedy, uint32_t flags);

@@ -291,7 +291,9 @@ __device__ int build_schedule(const RowJob& job, uint32_t* mask, uint16_t* pre, 
       // a child (a node after its parent) of a sampled tree
       if (ch == 0 || par[k] < 0 || par[k] >= ch || !(temp[k] > 0.0f)) continue;
       const int r = b * job.N + par[k];
-      if (r >= q_lo) atomicOr(&mask[r >> 5], 1u << (r & 31));
+      int word = r >> 5;
+      SPEC_CHECK_INDEX(word, kSchedWords, 16);
+      if (r >= q_lo) atomicOr(&mask[word], 1u << (r & 31));
     }
   }
   __syncthreads();
@@ -332,7 +334,9 @@ __device__ int build_schedule(const RowJob& job, uint32_t* mask, uint16_t* pre, 
       for (uint32_t k = t - pre[lo]; k > 0 && m; --k) m &= m - 1u;  // drop the lower bits
       v = BN + lo * 32 + (m ? __ffs(m) - 1 : 0);
     }
-    rows[i] = v;
+    int at = i;
+    SPEC_CHECK_INDEX(at, kSchedRows, 17);
+    rows[at] = v;
   }
   __syncthreads();
   return n_mine;
@@ -510,7 +514,9 @@ __global__ void __launch_bounds__(kBlockThreads, row_blocks<MODE>()) row_pass_ke
       }
       const int64_t off = (int64_t)b * job.batch_stride + (int64_t)n * job.row_pitch;
       row = row_ptr(is_q ? job.base_q : job.base_p, off, Elt<T>::kBytes);
-      out = (is_q ? job.stats_q : job.stats_p) + r;
+      int ro = r;
+      SPEC_CHECK_INDEX(ro, BN, 18);
+      out = (is_q ? job.stats_q : job.stats_p) + ro;
     }
     // the block-wide running maximum starts afresh for every row (all reads of the
     // previous row's value happened before that row's last barrier)
@@ -1074,6 +1080,20 @@ cudaError_t launch_row_pass(const RowJob& job, spec_dtype dtype, int num_rows, c
   if (mode == 0) return launch_mode<float, 0>(job, num_rows, s);
   if (mode == 1) return launch_mode<float, 1>(job, num_rows, s);
   return launch_mode<float, 2>(job, num_rows, s);
+}
+
+// Checked builds: this translation unit's error word, read and cleared (0 in other
+// builds).  Synchronous: it waits for the device.
+uint32_t check_word_rows() {
+#ifdef SPEC_CHECK
+  unsigned v = 0u;
+  const unsigned zero = 0u;
+  if (cudaMemcpyFromSymbol(&v, g_spec_check, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (cudaMemcpyToSymbol(g_spec_check, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+#else
+  return 0u;
+#endif
 }
 
 }  // namespace svk

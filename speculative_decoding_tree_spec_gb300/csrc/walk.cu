@@ -1346,9 +1346,14 @@ __device__ bool cluster_cut_sorted(const TreeJob& job, const void* prow, const v
       if (i < total[r]) {
         unsigned off = 0, q = 0;
         while (q + 1 < (unsigned)C && i >= off + cnt[r][q]) { off += cnt[r][q]; ++q; }
-        v = ld_peer_u64(peer_addr(cl[r] + (i - off), q));
+        unsigned li = i - off;
+        SPEC_CHECK_INDEX(li, kCandCTA, 0);
+        SPEC_CHECK_INDEX(q, C, 0);
+        v = ld_peer_u64(peer_addr(cl[r] + li, q));
       }
-      keys[i] = v;
+      unsigned ki = i;
+      SPEC_CHECK_INDEX(ki, kSortW, 1);
+      keys[ki] = v;
     }
   }
   __syncthreads();
@@ -1661,7 +1666,8 @@ __device__ bool cluster_cut_bf16(const TreeJob& job, const void* prow, const voi
           for (unsigned i = threadIdx.x; i < own_n[r]; i += CT) {
             const uint64_t e = cl[r][i];
             if ((uint32_t)(e >> 32) == cut32[r]) {
-              const unsigned pos = atomicAdd(&sh.mem_n[r], 1u);
+              unsigned pos = atomicAdd(&sh.mem_n[r], 1u);
+              SPEC_CHECK_INDEX(pos, kWalkBins, 8);
               merged[r][pos] = ~(uint32_t)e;
             }
           }
@@ -1840,7 +1846,11 @@ __device__ __noinline__ void tk_compact(uint64_t* list, unsigned n, unsigned K, 
   unsigned pos = warp_reserve(&sh.ncand[r], keep);
 #pragma unroll
   for (int t = 0; t < PER; ++t)
-    if (threadIdx.x + t * CT < n && (uint32_t)(mine[t] >> 32) >= thr) list[pos++] = mine[t];
+    if (threadIdx.x + t * CT < n && (uint32_t)(mine[t] >> 32) >= thr) {
+      unsigned at = pos++;
+      SPEC_CHECK_INDEX(at, n, 9);
+      list[at] = mine[t];
+    }
   __syncthreads();
 }
 
@@ -2097,9 +2107,14 @@ __device__ bool cluster_cut_topk(const TreeJob& job, const void* prow, const voi
       if (i < total[r]) {
         unsigned off = 0, q = 0;
         while (q + 1 < (unsigned)C && i >= off + cnt[r][q]) { off += cnt[r][q]; ++q; }
-        v = ld_peer_u64(peer_addr(list[r] + (i - off), q));
+        unsigned li = i - off;
+        SPEC_CHECK_INDEX(li, kCandCTA, 2);
+        SPEC_CHECK_INDEX(q, C, 2);
+        v = ld_peer_u64(peer_addr(list[r] + li, q));
       }
-      keys[i] = v;
+      unsigned ki = i;
+      SPEC_CHECK_INDEX(ki, kTkSort, 3);
+      keys[ki] = v;
     }
   }
   __syncthreads();
@@ -2361,8 +2376,9 @@ __device__ void build_kept(const TreeJob& job, const uint64_t* list_p, unsigned 
     const unsigned i = i0 + lane;
     const uint64_t w = i < n ? list_p[i] : 0ull;
     const bool in = i < n && w >= cutw;
-    const unsigned pos = warp_reserve(&sh.kp_n, in ? 1u : 0u);
+    unsigned pos = warp_reserve(&sh.kp_n, in ? 1u : 0u);
     if (in) {
+      SPEC_CHECK_INDEX(pos, kKeptCTA, 4);
       ks.idx[pos] = ~(uint32_t)w;
       ks.p[pos] = key_value((uint32_t)(w >> 32));
     }
@@ -2402,7 +2418,7 @@ __device__ bool kept_residual(const KeptSet& ks, unsigned nk, double* rz, float*
   const double z = tot * (1.0 / 4398046511104.0);
   if (threadIdx.x == 0) {
     const double r = z > 0.0 ? 1.0 / z : 0.0;
-    rz[j] = r;
+    rz[j] = r;  // j < N: one residual per child of the node at most
     invz[j] = z > 0.0 ? (float)r : -1.f;
   }
   __syncthreads();
@@ -2439,6 +2455,7 @@ __device__ int kept_draw(const KeptSet& ks, unsigned nk, double r, CShared& sh, 
     const uint32_t me = ks.idx[i];
     unsigned rk = 0;
     for (unsigned t = 0; t < nk; ++t) rk += (ks.idx[t] < me);
+    SPEC_CHECK_INDEX(rk, kKeptCTA, 5);
     order[rk] = i;
   }
   __syncthreads();
@@ -2702,8 +2719,10 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
       if (!cluster_sum(part, sh, C, rank, n_ex, z, nullptr)) { timed_out = true; break; }
       if (threadIdx.x == 0) {
         const double r = z > 0.0 ? 1.0 / z : 0.0;
-        rz[j] = r;
-        invz[j] = z > 0.0 ? (float)r : -1.f;
+        int jj = j;
+        SPEC_CHECK_INDEX(jj, N, 7);
+        rz[jj] = r;
+        invz[jj] = z > 0.0 ? (float)r : -1.f;
         if (lead && job.counters) {
           atomicAdd(&job.counters[2], 2ull * (unsigned long long)V * Elt<T>::kBytes);
           atomicAdd(&job.counters[3], 1ull);
@@ -2715,8 +2734,10 @@ __global__ void __launch_bounds__(CT, kWalkCtasPerSm) cluster_walk_kernel(TreeJo
     if (timed_out) { status = SPEC_ROW_TIMEOUT; break; }
     if (next >= 0) {
       if (lead && threadIdx.x == 0) {
-        out_tok[n_acc] = tok[next];
-        out_path[n_acc + 1] = next;
+        int at = n_acc;
+        SPEC_CHECK_INDEX(at, W - 1, 6);
+        out_tok[at] = tok[next];
+        out_path[at + 1] = next;
       }
       ++n_acc;
       u = next;
@@ -2860,6 +2881,9 @@ __global__ void __launch_bounds__(32 * kSmallWarps) small_walk_kernel(TreeJob jo
   const int N = job.N, V = job.V, W = job.W;
   int32_t* par = s_par[w];
   int32_t* tok = s_tok[w];
+  int n_max = N;
+  SPEC_CHECK_INDEX(n_max, kSmallMaxN + 1, 10);  // the dispatch admits N <= kSmallMaxN
+  if (n_max != N) return;
   for (int n = lane; n < N; n += 32) {
     par[n] = job.parents[(int64_t)b * N + n];
     tok[n] = job.tokens[(int64_t)b * N + n];
@@ -2932,8 +2956,10 @@ __global__ void __launch_bounds__(32 * kSmallWarps) small_walk_kernel(TreeJob jo
     }
     if (next >= 0) {
       if (lane == 0) {
-        out_tok[n_acc] = tok[next];
-        out_path[n_acc + 1] = next;
+        int at = n_acc;
+        SPEC_CHECK_INDEX(at, W - 1, 11);
+        out_tok[at] = tok[next];
+        out_path[at + 1] = next;
       }
       ++n_acc;
       u = next;
@@ -3067,6 +3093,20 @@ cudaError_t launch_philox_words(uint64_t seed, uint64_t offset, const int32_t* b
   if (n <= 0) return cudaSuccess;
   philox_words_kernel<<<(n + 255) / 256, 256, 0, s>>>(seed, offset, b_idx, node_idx, n, out);
   return cudaGetLastError();
+}
+
+// Checked builds: this translation unit's error word, read and cleared (0 in other
+// builds).  Synchronous: it waits for the device.
+uint32_t check_word_walk() {
+#ifdef SPEC_CHECK
+  unsigned v = 0u;
+  const unsigned zero = 0u;
+  if (cudaMemcpyFromSymbol(&v, g_spec_check, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (cudaMemcpyToSymbol(g_spec_check, &zero, sizeof(zero)) != cudaSuccess) return 0xffffffffu;
+  return v;
+#else
+  return 0u;
+#endif
 }
 
 }  // namespace svk

@@ -5,16 +5,22 @@
 // confidence -- its softmax probability at temperature T over the whole row -- which
 // the dynamic tree multiplies along a path.
 //
-// One 256-thread CTA per row.  Each lane takes kDraftUnroll 16-byte units of the row
-// per round (one load each, all in flight) and keeps the running maximum and the Kahan
-// sum of 2^((z - max) c), c = log2(e)/T, rescaled when the maximum grows (the row
-// pass's normaliser; the weights by packed fp32 FMAs).  Each warp keeps the K largest
-// order keys it has seen (logit order bits, then the complement of the index: a larger
-// key is a larger logit or, on a tie, a lower index), lane j holding the j-th.  Per
-// round one ballot asks which lanes' units reach the list's last logit (packed bf16
-// maxima); only their elements are offered to the list, one at a time by shuffles,
-// so after the first few rounds almost no round inserts anything.  The 8 warp lists
-// are merged by counting, for each key, the keys above it.
+// One 192-thread CTA per row, five per SM (so 640 rows of the full vocabulary fit in one
+// wave of 152 SMs).  Each lane takes kDraftUnroll 16-byte units of the row per round
+// (one load each, all in flight, the next round's issued before this round's
+// arithmetic) and keeps the running maximum and the Kahan sum of 2^((z - max) c),
+// c = log2(e)/T, rescaled when the maximum grows (the row pass's normaliser; the
+// weights by packed fp32 FMAs).  The CTA keeps one list of the row's largest order keys
+// (logit order bits, then the complement of the index: a larger key is a larger logit
+// or, on a tie, a lower index) in shared memory.  A round covers a contiguous block of
+// units, so every element of a later round has a larger index than every listed key and
+// only elements strictly above the list's k-th logit can place: a lane offers those
+// (packed bf16 compares against the threshold) to the round's candidate buffer, and
+// one warp, a different one each round, merges that buffer into the list during the
+// next round (bitonic merges across the warp's lanes).  The first round is seeded with
+// a floor (the k-th largest lane maximum) and merged before the second starts.  A
+// round that offers more candidates than the buffer holds merges it at once and
+// offers the rest again against the raised list.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -23,10 +29,11 @@ namespace svk {
 
 namespace {
 
-constexpr int kDraftThreads = 256;
+constexpr int kDraftThreads = 192;
 constexpr int kDraftWarps = kDraftThreads / 32;
 constexpr int kDraftUnroll = 4;
 constexpr int kDraftMaxK = 32;
+constexpr int kDraftCap = 512;  // candidate keys a round's buffer holds
 
 struct DraftJob {
   const void* base;
@@ -95,9 +102,10 @@ __device__ __forceinline__ float units_max(const uint4 (&raw)[kDraftUnroll]) {
   }
 }
 
-// Candidate bits of a lane's units: element e of unit k (bit k E + e) is not below
-// thr.  bf16: two logits per compare, against thr (a bf16 value, exact).
-template <typename T>
+// Candidate bits of a lane's units: bit k E + e is set when element e of unit k is
+// above thr (kStrict) or not below it.  bf16: two logits per compare, against thr (a
+// bf16 value, exact).
+template <typename T, bool kStrict>
 __device__ __forceinline__ uint32_t candidate_bits(const uint4 (&raw)[kDraftUnroll], float thr) {
   uint32_t bits = 0u;
   if constexpr (sizeof(T) == 2) {
@@ -107,7 +115,7 @@ __device__ __forceinline__ uint32_t candidate_bits(const uint4 (&raw)[kDraftUnro
       const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const unsigned m = __hge2_mask(as_bf2(w[q]), t2);
+        const unsigned m = kStrict ? __hgt2_mask(as_bf2(w[q]), t2) : __hge2_mask(as_bf2(w[q]), t2);
         bits |= ((m & 1u) | ((m >> 15) & 2u)) << (k * 8 + 2 * q);
       }
     }
@@ -116,10 +124,62 @@ __device__ __forceinline__ uint32_t candidate_bits(const uint4 (&raw)[kDraftUnro
     for (int k = 0; k < kDraftUnroll; ++k) {
       const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) bits |= (uint32_t)(!(__uint_as_float(w[q]) < thr)) << (k * 4 + q);
+      for (int q = 0; q < 4; ++q) {
+        const float v = __uint_as_float(w[q]);
+        bits |= (uint32_t)(kStrict ? (v > thr) : !(v < thr)) << (k * 4 + q);
+      }
     }
   }
   return bits;
+}
+
+// 64-bit keys held one per lane, sorted descending by a bitonic network (blocks of
+// size s alternate direction so that each pair forms a bitonic sequence; size 32 is
+// descending).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t y = __shfl_xor_sync(kFull, x, stride);
+      const bool desc = (lane & size) == 0, low = (lane & stride) == 0;
+      x = (low == desc) ? (x > y ? x : y) : (x < y ? x : y);
+    }
+  }
+  return x;
+}
+
+// The row's list (32 keys, descending, lane j holding the j-th) merged with n keys of a
+// candidate buffer by one whole warp.  A chunk of up to 32 keys is sorted, reversed
+// against the list (the lane-wise larger of the list and the reversed chunk holds the
+// 32 largest of both, as a bitonic sequence) and merged; a chunk of a few keys is
+// inserted one key at a time instead.  Returns the merged list.
+__device__ uint64_t merge_into_list(uint64_t L, const uint64_t* buf, int n, int k_out, int lane) {
+  for (int c = 0; c < n; c += 32) {
+    const int m = min(32, n - c);
+    if (m <= 6) {
+      for (int i = 0; i < m; ++i) {
+        const uint64_t x = buf[c + i];
+        const int pos = __popc(__ballot_sync(kFull, L > x));
+        if (pos < k_out) {
+          const uint64_t up = __shfl_up_sync(kFull, L, 1);
+          if (lane > pos) L = up;
+          if (lane == pos) L = x;
+        }
+      }
+    } else {
+      uint64_t x = lane < m ? buf[c + lane] : 0ull;
+      x = warp_sort_desc(x, lane);
+      const uint64_t y = __shfl_sync(kFull, x, 31 - lane);
+      L = L > y ? L : y;
+#pragma unroll
+      for (int stride = 16; stride > 0; stride >>= 1) {
+        const uint64_t o = __shfl_xor_sync(kFull, L, stride);
+        L = ((lane & stride) == 0) == (L > o) ? L : o;
+      }
+    }
+  }
+  return L;
 }
 
 // A lane's U units of the round starting at unit u0 (padding past V is -inf).
@@ -142,17 +202,58 @@ __device__ __forceinline__ void load_round(const void* row, int V, int nunits, i
   }
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job) {
+// The key of element idx of a row: its logit's order bits, then the complement of idx.
+template <typename T>
+__device__ __forceinline__ uint64_t element_key(const void* row, int idx) {
+  const float z = Elt<T>::at(row, idx);
+  return ((uint64_t)order_key(z) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+// A lane's candidates (bits of its units in the round at u0) into the round's buffer;
+// those past its capacity are returned as still pending.  With lk != 0 only keys above
+// lk (the list's k-th key) are kept.
+template <typename T>
+__device__ __forceinline__ uint32_t append_candidates(const void* row, uint32_t bits, int u0, int lane,
+                                                      uint64_t lk, uint64_t* buf, int* cnt) {
+  constexpr int E = Elt<T>::kPerUnit;
+  uint32_t keep = bits;
+  if (lk != 0ull) {
+    uint32_t b = bits;
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      b &= b - 1;
+      const int idx = (u0 + lane + (bit / E) * kDraftThreads) * E + bit % E;
+      if (!(element_key<T>(row, idx) > lk)) keep &= ~(1u << bit);
+    }
+  }
+  if (!keep) return 0u;
+  int slot = atomicAdd(cnt, __popc(keep));
+  uint32_t pend = 0u;
+  while (keep) {
+    const int bit = __ffs(keep) - 1;
+    keep &= keep - 1;
+    if (slot < kDraftCap) {
+      const int idx = (u0 + lane + (bit / E) * kDraftThreads) * E + bit % E;
+      buf[slot] = element_key<T>(row, idx);
+    } else {
+      pend |= 1u << bit;
+    }
+    ++slot;
+  }
+  return pend;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDraftThreads, 5) draft_topk_kernel(DraftJob job) {
   constexpr int E = Elt<T>::kPerUnit;
   constexpr int U = kDraftUnroll;
-  __shared__ uint64_t wlist[kDraftWarps * K];
-  __shared__ uint64_t fin[K];
+  __shared__ uint64_t s_list[32];               // the row's largest keys so far, descending
+  __shared__ uint64_t s_buf[2][kDraftCap];      // candidates of a round, by round parity
+  __shared__ int s_cnt[2];
+  __shared__ unsigned s_thr;  // order key of a logit that nothing later at or below it can beat
   __shared__ float wmax[kDraftWarps];
   __shared__ double wsum[kDraftWarps];
   __shared__ float s_m;
-  __shared__ unsigned s_cut;  // order key of the largest warp threshold published so far
-  __shared__ __align__(16) uint4 stage[kDraftWarps][U][32];  // a round's units, for candidates
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x;
   const void* row = static_cast<const char*>(job.base) + (int64_t)r * job.pitch_bytes;
@@ -160,30 +261,38 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
   const int nunits = (V + E - 1) / E, full_units = V / E;
   const float c = job.c;
   const float2 c2 = make_float2(c, c);
+  const int step = kDraftThreads * U;  // units of one round: round q covers [q step, (q+1) step)
+  const int nrounds = (nunits + step - 1) / step;
 
-  // the warp's list: lane j < k holds its j-th largest key (0 = empty); only the first
-  // k places matter (the row's k largest are among every warp's k largest)
-  uint64_t wkey = 0ull;
-  bool full = false;           // warp-uniform: the list holds k keys
-  float thr = -CUDART_INF_F;   // warp-uniform: the logit of its k-th key once full
-  float lo = -CUDART_INF_F;    // warp-uniform: a floor below which nothing can place
+  if (threadIdx.x < 32) s_list[threadIdx.x] = 0ull;  // 0 is below every key
+  if (threadIdx.x < 2) s_cnt[threadIdx.x] = 0;
+  if (threadIdx.x == 0) s_thr = order_key(-CUDART_INF_F);
+  __syncthreads();
+
   float m = -CUDART_INF_F;
   Kahan s;
   int bad = 0;
-  const int step = kDraftThreads * U;
-  // a warp whose list is full holds k elements at or above its threshold, so nothing
-  // below the largest threshold of any warp can place: the warps share it
-  if (threadIdx.x == 0) s_cut = order_key(-CUDART_INF_F);
-  __syncthreads();
   uint4 raw[U], nxt[U];
-  int u0 = warp * 32;
-  if (u0 < nunits) load_round<T>(row, V, nunits, full_units, u0, lane, nxt);
-  // every lane runs the same number of rounds (the ballots below need the whole warp);
-  // the next round's loads are issued before this round's arithmetic
-  for (; u0 < nunits; u0 += step) {
+  load_round<T>(row, V, nunits, full_units, warp * 32, lane, nxt);
+  for (int q = 0; q < nrounds; ++q) {
+    const int u0 = q * step + warp * 32;
+    const int b = q & 1;
+    // the previous round's candidates join the list (one warp, a different one each round)
+    if (warp == q % kDraftWarps) {
+      const int n = min(s_cnt[b ^ 1], kDraftCap);
+      if (n > 0) {
+        const uint64_t L = merge_into_list(s_list[lane], s_buf[b ^ 1], n, k_out, lane);
+        s_list[lane] = L;
+        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
+        if (lane == 0) {
+          s_cnt[b ^ 1] = 0;
+          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
+        }
+      }
+    }
 #pragma unroll
     for (int k = 0; k < U; ++k) raw[k] = nxt[k];
-    if (u0 + step < nunits) load_round<T>(row, V, nunits, full_units, u0 + step, lane, nxt);
+    if (q + 1 < nrounds) load_round<T>(row, V, nunits, full_units, u0 + step, lane, nxt);
     const float um = units_max<T>(raw);
     bad |= (um != um);
     if (um > m) {
@@ -213,9 +322,10 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
       s.add(tot.x + tot.y);
     }
 
-    if (!full) {
-      // until the list is full: a floor from this round, the k-th largest lane maximum
-      // (k lanes hold an element at least this large, so nothing below it can place)
+    uint32_t pend = 0u;
+    if (q == 0) {
+      // a floor: per warp the k-th largest lane maximum (k lanes hold an element at least
+      // this large), the largest over the warps; every element at or above it is offered
       const float v = (um != um) ? -CUDART_INF_F : um;
       int above = 0;
 #pragma unroll 8
@@ -223,14 +333,9 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
         const float o = __shfl_sync(kFull, v, j);
         above += (o > v) || (o == v && j < lane);
       }
-      const unsigned at = __ballot_sync(kFull, above == k_out - 1);
-      if (at) lo = fmaxf(lo, __shfl_sync(kFull, v, __ffs(at) - 1));
-    }
-    // offer the elements that reach the list's last logit (padding past V never)
-    const float cut = fmaxf(full ? fmaxf(thr, lo) : lo, key_value(*(volatile unsigned*)&s_cut));
-    if (!__any_sync(kFull, !(um < cut))) continue;
-    uint32_t cand = 0u;
-    if (!(um < cut)) {
+      if (above == k_out - 1) atomicMax(&s_thr, order_key(v));
+      __syncthreads();
+      const float fl = key_value(s_thr);
       uint32_t valid = 0xFFFFFFFFu;
       if (u0 + 32 + (U - 1) * kDraftThreads > full_units) {
         valid = 0u;
@@ -241,60 +346,71 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
           valid |= (uint32_t)((1ull << n_in) - 1ull) << (k * E);
         }
       }
-      cand = candidate_bits<T>(raw, cut) & valid;
-    }
-#pragma unroll
-    for (int k = 0; k < U; ++k) stage[warp][k][lane] = raw[k];
-    __syncwarp();
-    unsigned bal = __ballot_sync(kFull, cand != 0u);
-    while (bal) {
-      const int src = __ffs(bal) - 1;
-      bal &= bal - 1;
-      uint32_t bits = __shfl_sync(kFull, cand, src);
-      while (bits) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int k = bit / E, e = bit % E;
-        const float z = sizeof(T) == 2
-            ? __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(&stage[warp][k][src])[e] << 16)
-            : reinterpret_cast<const float*>(&stage[warp][k][src])[e];
-        if (full && z < thr) continue;  // the list moved on meanwhile (warp-uniform)
-        const int idx = (u0 + src + k * kDraftThreads) * E + e;
-        const uint64_t x =
-            ((uint64_t)order_key(z) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)idx);
-        // the lanes holding larger keys are a prefix of the list
-        const int pos = __popc(__ballot_sync(kFull, lane < k_out && wkey > x));
-        if (pos < k_out) {
-          const uint64_t up = __shfl_up_sync(kFull, wkey, 1);
-          if (lane > pos && lane < k_out) wkey = up;
-          if (lane == pos) wkey = x;
-          const uint64_t last = __shfl_sync(kFull, wkey, k_out - 1);
-          full = last != 0ull;
-          thr = key_value((uint32_t)(last >> 32));
-        }
+      const uint32_t cand = (um != um || um < fl) ? 0u : candidate_bits<T, false>(raw, fl) & valid;
+      pend = append_candidates<T>(row, cand, u0, lane, 0ull, s_buf[0], &s_cnt[0]);
+    } else {
+      // later rounds hold larger indices than every listed key, so an element must lie
+      // strictly above the threshold to place; the threshold may lag the list
+      const float thr = key_value(*(volatile unsigned*)&s_thr);
+      if (__any_sync(kFull, um > thr)) {
+        const uint32_t cand = um > thr ? candidate_bits<T, true>(raw, thr) : 0u;
+        pend = append_candidates<T>(row, cand, u0, lane, 0ull, s_buf[b], &s_cnt[b]);
       }
     }
-    if (full && lane == 0) atomicMax(&s_cut, order_key(thr));
-    __syncwarp();
+    __syncthreads();
+    // a round with more candidates than the buffer holds: the buffer joins the list, then
+    // the pending ones above the list's k-th key are offered again (every pass takes in
+    // a full buffer or clears every pending element, so at most step E / cap passes)
+    int n = s_cnt[b];
+    for (int pass = 0; n > kDraftCap && pass <= step * E / kDraftCap; ++pass) {
+      __syncthreads();  // every thread has read n
+      if (warp == 0) {
+        const uint64_t L = merge_into_list(s_list[lane], s_buf[b], kDraftCap, k_out, lane);
+        s_list[lane] = L;
+        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
+        if (lane == 0) {
+          s_cnt[b] = 0;
+          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
+        }
+      }
+      __syncthreads();
+      const uint64_t lk = s_list[k_out - 1];
+      pend = append_candidates<T>(row, pend, u0, lane, lk, s_buf[b], &s_cnt[b]);
+      __syncthreads();
+      n = s_cnt[b];
+    }
+    if (q == 0) {
+      // the first round joins the list before the next one starts (the threshold from
+      // the floor alone would let far more of it through)
+      if (warp == 0) {
+        const int n0 = min(s_cnt[0], kDraftCap);
+        const uint64_t L = merge_into_list(s_list[lane], s_buf[0], n0, k_out, lane);
+        s_list[lane] = L;
+        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
+        if (lane == 0) {
+          s_cnt[0] = 0;
+          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // the last round's candidates
+  if (nrounds > 1 && warp == 0) {
+    const int b = (nrounds - 1) & 1;
+    const int n = min(s_cnt[b], kDraftCap);
+    if (n > 0) s_list[lane] = merge_into_list(s_list[lane], s_buf[b], n, k_out, lane);
   }
 
   // the row's maximum and normaliser
   bad = __syncthreads_or(bad);
   const float wm = warp_max(m);
   if (lane == 0) wmax[warp] = wm;
-  if (lane < K) wlist[warp * K + lane] = lane < k_out ? wkey : 0ull;
   __syncthreads();
   if (threadIdx.x == 0) {
     float M = -CUDART_INF_F;
     for (int w = 0; w < kDraftWarps; ++w) M = fmaxf(M, wmax[w]);
     s_m = M;
-  }
-  // the k largest of the warps' keys: a key's place is the number of keys above it
-  if ((int)threadIdx.x < kDraftWarps * K) {
-    const uint64_t mine = wlist[threadIdx.x];
-    int above = 0;
-    for (int j = 0; j < kDraftWarps * K; ++j) above += wlist[j] > mine;
-    if (mine != 0ull && above < k_out) fin[above] = mine;
   }
   __syncthreads();
   const float M = s_m;
@@ -314,7 +430,7 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
     double S = 0.0;
     for (int w = 0; w < kDraftWarps; ++w) S += wsum[w];
     const int t = threadIdx.x;
-    const uint64_t key = fin[t];
+    const uint64_t key = s_list[t];
     int32_t tok = -1;
     float p = 0.f;
     if (finite) {
@@ -332,9 +448,7 @@ __global__ void __launch_bounds__(kDraftThreads) draft_topk_kernel(DraftJob job)
 
 template <typename T>
 cudaError_t launch_draft(const DraftJob& job, cudaStream_t s) {
-  if (job.k <= 8) draft_topk_kernel<T, 8><<<job.R, kDraftThreads, 0, s>>>(job);
-  else if (job.k <= 16) draft_topk_kernel<T, 16><<<job.R, kDraftThreads, 0, s>>>(job);
-  else draft_topk_kernel<T, 32><<<job.R, kDraftThreads, 0, s>>>(job);
+  draft_topk_kernel<T><<<job.R, kDraftThreads, 0, s>>>(job);
   return cudaGetLastError();
 }
 

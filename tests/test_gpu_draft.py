@@ -83,3 +83,34 @@ def test_draft_topk_full_size_sampled():
         assert out["tokens"][r].cpu().tolist() == tok[0].tolist(), r
         gp = out["probs"][r].cpu().numpy().astype(np.float64)
         assert np.max(np.abs(gp - prob[0]) / prob[0]) <= 1e-5, r
+
+
+def _adversarial(R_kind, V, dtype):
+    """Rows whose largest logits arrive late, all at once, or tied in the thousands."""
+    g = torch.Generator(device="cpu").manual_seed(11)
+    if R_kind == "ascending":      # every later block beats all earlier ones
+        x = torch.linspace(-8.0, 8.0, V).repeat(2, 1)
+    elif R_kind == "descending":
+        x = torch.linspace(8.0, -8.0, V).repeat(2, 1)
+    elif R_kind == "constant":     # one value: the lowest indices win
+        x = torch.full((2, V), 1.25)
+    elif R_kind == "two_level":    # a few hundred tied maxima scattered over the row
+        x = torch.zeros((2, V))
+        x[torch.rand((2, V), generator=g) < 0.003] = 1.0
+    elif R_kind == "late":         # the largest logits all in the row's last stretch
+        x = torch.randn((2, V), generator=g)
+        x[:, V - 3000:] += 6.0
+    else:
+        raise ValueError(R_kind)
+    return x.to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("kind", ["ascending", "descending", "constant", "two_level", "late"])
+def test_draft_topk_adversarial_orders(dtype, kind):
+    """Full-vocabulary rows where a block of a round offers more candidates than the
+    kernel's per-round buffer, or where every round raises the list: children still
+    bit-exact with ties to the lower index."""
+    x = _adversarial(kind, 128256, dtype)
+    for k in (1, 10, 32):
+        _check(x, k, 1.0)

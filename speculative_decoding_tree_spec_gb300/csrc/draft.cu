@@ -15,12 +15,13 @@
 // or, on a tie, a lower index) in shared memory.  A round covers a contiguous block of
 // units, so every element of a later round has a larger index than every listed key and
 // only elements strictly above the list's k-th logit can place: a lane offers those
-// (packed bf16 compares against the threshold) to the round's candidate buffer, and
-// one warp, a different one each round, merges that buffer into the list during the
-// next round (bitonic merges across the warp's lanes).  The first round is seeded with
-// a floor (the k-th largest lane maximum) and merged before the second starts.  A
-// round that offers more candidates than the buffer holds merges it at once and
-// offers the rest again against the raised list.
+// (packed bf16 compares against the threshold) to a candidate buffer shared by a group
+// of kDraftGroup rounds (one barrier per group), and one warp, a different one each
+// group, merges that buffer into the list while the next group streams (bitonic merges
+// across the warp's lanes).  The first round is seeded with a floor (the k-th largest
+// lane maximum) and merged before the second starts.  A group that offers more
+// candidates than the buffer holds merges it at once and offers the rest again against
+// the raised list.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -33,7 +34,8 @@ constexpr int kDraftThreads = 192;
 constexpr int kDraftWarps = kDraftThreads / 32;
 constexpr int kDraftUnroll = 4;
 constexpr int kDraftMaxK = 32;
-constexpr int kDraftCap = 512;  // candidate keys a round's buffer holds
+constexpr int kDraftCap = 512;  // candidate keys a group's buffer holds
+constexpr int kDraftGroup = 2;  // rounds between two barriers
 
 struct DraftJob {
   const void* base;
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kDraftThreads, 5) draft_topk_kernel(DraftJob j
   constexpr int E = Elt<T>::kPerUnit;
   constexpr int U = kDraftUnroll;
   __shared__ uint64_t s_list[32];               // the row's largest keys so far, descending
-  __shared__ uint64_t s_buf[2][kDraftCap];      // candidates of a round, by round parity
+  __shared__ uint64_t s_buf[2][kDraftCap];      // candidates of a group of rounds, by its parity
   __shared__ int s_cnt[2];
   __shared__ unsigned s_thr;  // order key of a logit that nothing later at or below it can beat
   __shared__ float wmax[kDraftWarps];
@@ -273,26 +275,13 @@ __global__ void __launch_bounds__(kDraftThreads, 5) draft_topk_kernel(DraftJob j
   Kahan s;
   int bad = 0;
   uint4 raw[U], nxt[U];
-  load_round<T>(row, V, nunits, full_units, warp * 32, lane, nxt);
-  for (int q = 0; q < nrounds; ++q) {
-    const int u0 = q * step + warp * 32;
-    const int b = q & 1;
-    // the previous round's candidates join the list (one warp, a different one each round)
-    if (warp == q % kDraftWarps) {
-      const int n = min(s_cnt[b ^ 1], kDraftCap);
-      if (n > 0) {
-        const uint64_t L = merge_into_list(s_list[lane], s_buf[b ^ 1], n, k_out, lane);
-        s_list[lane] = L;
-        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
-        if (lane == 0) {
-          s_cnt[b ^ 1] = 0;
-          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
-        }
-      }
-    }
+
+  // round q: the units loaded last round become this round's, the next round's loads go
+  // out, then the running maximum and normaliser; returns the lane's maximum
+  auto stream = [&](int q) -> float {
 #pragma unroll
     for (int k = 0; k < U; ++k) raw[k] = nxt[k];
-    if (q + 1 < nrounds) load_round<T>(row, V, nunits, full_units, u0 + step, lane, nxt);
+    if (q + 1 < nrounds) load_round<T>(row, V, nunits, full_units, (q + 1) * step + warp * 32, lane, nxt);
     const float um = units_max<T>(raw);
     bad |= (um != um);
     if (um > m) {
@@ -321,83 +310,106 @@ __global__ void __launch_bounds__(kDraftThreads, 5) draft_topk_kernel(DraftJob j
       const float2 tot = __fadd2_rn(acc[0], acc[1]);
       s.add(tot.x + tot.y);
     }
-
-    uint32_t pend = 0u;
-    if (q == 0) {
-      // a floor: per warp the k-th largest lane maximum (k lanes hold an element at least
-      // this large), the largest over the warps; every element at or above it is offered
-      const float v = (um != um) ? -CUDART_INF_F : um;
-      int above = 0;
-#pragma unroll 8
-      for (int j = 0; j < 32; ++j) {
-        const float o = __shfl_sync(kFull, v, j);
-        above += (o > v) || (o == v && j < lane);
-      }
-      if (above == k_out - 1) atomicMax(&s_thr, order_key(v));
+    return um;
+  };
+  // buffer bb joins the list (a whole warp); its count is cleared and the threshold raised
+  auto merge_buffer = [&](int bb, int n) {
+    const uint64_t L = merge_into_list(s_list[lane], s_buf[bb], n, k_out, lane);
+    s_list[lane] = L;
+    const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
+    if (lane == 0) {
+      s_cnt[bb] = 0;
+      if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
+    }
+  };
+  // a group that offered more candidates than buffer bb holds: the buffer joins the list,
+  // then the pending ones above the list's k-th key are offered again (every pass takes in
+  // a full buffer or clears every pending element, so the pass count is bounded by the
+  // group's elements over the capacity).  Every thread calls it after a barrier.
+  auto drain_overflow = [&](int bb, uint32_t (&pend)[kDraftGroup], int q0, int ng) {
+    int n = s_cnt[bb];
+    for (int pass = 0; n > kDraftCap && pass <= kDraftGroup * step * E / kDraftCap; ++pass) {
+      __syncthreads();  // every thread has read n
+      if (warp == 0) merge_buffer(bb, kDraftCap);
       __syncthreads();
-      const float fl = key_value(s_thr);
-      uint32_t valid = 0xFFFFFFFFu;
-      if (u0 + 32 + (U - 1) * kDraftThreads > full_units) {
-        valid = 0u;
+      const uint64_t lk = s_list[k_out - 1];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int u = u0 + lane + k * kDraftThreads;
-          const int n_in = min(max(V - u * E, 0), E);  // elements of this unit below V
-          valid |= (uint32_t)((1ull << n_in) - 1ull) << (k * E);
-        }
+      for (int j = 0; j < kDraftGroup; ++j)
+        if (j < ng)
+          pend[j] = append_candidates<T>(row, pend[j], (q0 + j) * step + warp * 32, lane, lk, s_buf[bb],
+                                         &s_cnt[bb]);
+      __syncthreads();
+      n = s_cnt[bb];
+    }
+  };
+
+  load_round<T>(row, V, nunits, full_units, warp * 32, lane, nxt);
+  {
+    // the first round: a floor, per warp the k-th largest lane maximum (k lanes hold an
+    // element at least this large), the largest over the warps; every element at or
+    // above it is offered, and the list takes them in before the next round starts
+    const int u0 = warp * 32;
+    const float um = stream(0);
+    const float v = (um != um) ? -CUDART_INF_F : um;
+    int above = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const float o = __shfl_sync(kFull, v, j);
+      above += (o > v) || (o == v && j < lane);
+    }
+    if (above == k_out - 1) atomicMax(&s_thr, order_key(v));
+    __syncthreads();
+    const float fl = key_value(s_thr);
+    uint32_t valid = 0xFFFFFFFFu;
+    if (u0 + 32 + (U - 1) * kDraftThreads > full_units) {
+      valid = 0u;
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int u = u0 + lane + k * kDraftThreads;
+        const int n_in = min(max(V - u * E, 0), E);  // elements of this unit below V
+        valid |= (uint32_t)((1ull << n_in) - 1ull) << (k * E);
       }
-      const uint32_t cand = (um != um || um < fl) ? 0u : candidate_bits<T, false>(raw, fl) & valid;
-      pend = append_candidates<T>(row, cand, u0, lane, 0ull, s_buf[0], &s_cnt[0]);
-    } else {
-      // later rounds hold larger indices than every listed key, so an element must lie
-      // strictly above the threshold to place; the threshold may lag the list
-      const float thr = key_value(*(volatile unsigned*)&s_thr);
-      if (__any_sync(kFull, um > thr)) {
-        const uint32_t cand = um > thr ? candidate_bits<T, true>(raw, thr) : 0u;
-        pend = append_candidates<T>(row, cand, u0, lane, 0ull, s_buf[b], &s_cnt[b]);
+    }
+    uint32_t pend[kDraftGroup];
+#pragma unroll
+    for (int j = 0; j < kDraftGroup; ++j) pend[j] = 0u;
+    const uint32_t cand = (um != um || um < fl) ? 0u : candidate_bits<T, false>(raw, fl) & valid;
+    pend[0] = append_candidates<T>(row, cand, u0, lane, 0ull, s_buf[0], &s_cnt[0]);
+    __syncthreads();
+    drain_overflow(0, pend, 0, 1);
+    if (warp == 0) merge_buffer(0, min(s_cnt[0], kDraftCap));
+    __syncthreads();
+  }
+  // later rounds, kDraftGroup to a barrier: their elements hold larger indices than every
+  // listed key, so an element must lie strictly above the threshold to place (the
+  // threshold may lag the list); group g offers into buffer g & 1, which one warp, a
+  // different one each group, merges into the list while the next group streams
+  for (int g = 0, q0 = 1; q0 < nrounds; ++g, q0 += kDraftGroup) {
+    const int b = g & 1;
+    if (warp == g % kDraftWarps) {
+      const int n = min(s_cnt[b ^ 1], kDraftCap);
+      if (n > 0) merge_buffer(b ^ 1, n);
+    }
+    uint32_t pend[kDraftGroup];
+#pragma unroll
+    for (int j = 0; j < kDraftGroup; ++j) {
+      pend[j] = 0u;
+      const int q = q0 + j;
+      if (q < nrounds) {
+        const float um = stream(q);
+        const float thr = key_value(*(volatile unsigned*)&s_thr);
+        if (__any_sync(kFull, um > thr)) {
+          const uint32_t cand = um > thr ? candidate_bits<T, true>(raw, thr) : 0u;
+          pend[j] = append_candidates<T>(row, cand, q * step + warp * 32, lane, 0ull, s_buf[b], &s_cnt[b]);
+        }
       }
     }
     __syncthreads();
-    // a round with more candidates than the buffer holds: the buffer joins the list, then
-    // the pending ones above the list's k-th key are offered again (every pass takes in
-    // a full buffer or clears every pending element, so at most step E / cap passes)
-    int n = s_cnt[b];
-    for (int pass = 0; n > kDraftCap && pass <= step * E / kDraftCap; ++pass) {
-      __syncthreads();  // every thread has read n
-      if (warp == 0) {
-        const uint64_t L = merge_into_list(s_list[lane], s_buf[b], kDraftCap, k_out, lane);
-        s_list[lane] = L;
-        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
-        if (lane == 0) {
-          s_cnt[b] = 0;
-          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
-        }
-      }
-      __syncthreads();
-      const uint64_t lk = s_list[k_out - 1];
-      pend = append_candidates<T>(row, pend, u0, lane, lk, s_buf[b], &s_cnt[b]);
-      __syncthreads();
-      n = s_cnt[b];
-    }
-    if (q == 0) {
-      // the first round joins the list before the next one starts (the threshold from
-      // the floor alone would let far more of it through)
-      if (warp == 0) {
-        const int n0 = min(s_cnt[0], kDraftCap);
-        const uint64_t L = merge_into_list(s_list[lane], s_buf[0], n0, k_out, lane);
-        s_list[lane] = L;
-        const uint64_t lk = __shfl_sync(kFull, L, k_out - 1);
-        if (lane == 0) {
-          s_cnt[0] = 0;
-          if (lk != 0ull) atomicMax(&s_thr, (unsigned)(lk >> 32));
-        }
-      }
-      __syncthreads();
-    }
+    drain_overflow(b, pend, q0, min(kDraftGroup, nrounds - q0));
   }
-  // the last round's candidates
+  // the last group's candidates
   if (nrounds > 1 && warp == 0) {
-    const int b = (nrounds - 1) & 1;
+    const int b = ((nrounds - 2) / kDraftGroup) & 1;
     const int n = min(s_cnt[b], kDraftCap);
     if (n > 0) s_list[lane] = merge_into_list(s_list[lane], s_buf[b], n, k_out, lane);
   }
